@@ -1,0 +1,19 @@
+"""B300-native softmax-attention prefix scan (Aaren many-to-many output).
+
+The compute path is the CUDA library libaaren.so (built for sm_103a, C ABI in
+include/aaren.h).  The Python binding in `binding` only marshals torch tensors
+into that ABI; importing this package does not load the library, the first
+call does, and it raises if the library is missing (there is no CPU fallback).
+"""
+
+__all__ = ["binding", "inputs"]
+
+
+def __getattr__(name):
+    if name == "binding":
+        from . import binding
+        return binding
+    if name == "inputs":
+        from . import inputs
+        return inputs
+    raise AttributeError(name)

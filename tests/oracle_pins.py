@@ -1,0 +1,286 @@
+"""Pins for the float64 oracle: checks against things other than the oracle.
+
+Each pin_* function raises AssertionError on failure.  tests/test_oracle.py
+runs them against the real oracle, and against deliberately broken copies of
+oracle.c to show that each plausible mistake (a dropped term, a wrong sign, a
+wrong index, a transposed operand) fails at least one pin.
+
+What pins what:
+  worked example   hand-derived rational example of the definition
+                   (tests/golden/rational_worked_example.txt)
+  brute force      per-prefix textbook softmax on tiny inputs
+  last row         o_N equals single-query softmax attention, computed with
+                   numpy's matmul and scipy.special.softmax
+  scores           q . k_t equals numpy's matmul
+  shift            adding a constant to every score leaves O unchanged and
+                   shifts m by that constant
+  equal scores     q = 0 gives the prefix means cumsum(V)/t
+  Hillis-Steele    the parallel-scan order of the same operator agrees
+  operator laws    associativity, commutativity, identity
+  first output     o_1 = v_1
+  one-hot          a score 60 above the rest makes o_t that token's v
+  bounds           o_t inside the convex hull of v_1..v_t, 1 <= w <= N,
+                   m = max s
+  long double      the same recurrence in long double agrees to ~1e-14
+  large scores     |s| up to 5000 (exp would overflow without rescaling)
+  continuation     scanning [A; B] equals scanning B from A's final state
+  running sum      the unscaled running sums of the memory-efficient-attention
+                   review (section 2) agree when the scores are moderate
+"""
+import os
+from fractions import Fraction
+
+import numpy as np
+import scipy.special
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _rng(seed):
+    return np.random.default_rng(seed)
+
+
+def _rel(a, b):
+    a, b = np.asarray(a, np.float64), np.asarray(b, np.float64)
+    return float(np.max(np.abs(a - b)) / max(1e-300, float(np.max(np.abs(b)))))
+
+
+def read_fixture(name):
+    vals = {}
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            key, rest = line.split(":", 1)
+            rows = [[Fraction(x) for x in r.split()] for r in rest.split("|")]
+            vals[key.strip()] = rows
+    return vals
+
+
+def pin_worked_example():
+    fx = read_fixture("rational_worked_example.txt")
+    e = [float(x) for x in fx["scores_exp"][0]]
+    s = np.log(np.array(e))
+    V = np.array([[float(x) for x in r] for r in fx["V"]], dtype=np.float32)
+    want = np.array([[float(x) for x in r] for r in fx["O"]])
+    O, m, u, w = oracle.scan_scores(s, V)
+    assert np.max(np.abs(O - want)) < 1e-14, (O, want)
+    assert abs(np.exp(m) - float(fx["m_exp"][0][0])) < 1e-13
+    assert abs(w - float(fx["w"][0][0])) < 1e-14
+    assert np.max(np.abs(u - np.array([float(x) for x in fx["u"][0]]))) < 1e-14
+    for alt in (oracle.bruteforce(s, V), oracle.hillis_steele(s, V)):
+        assert np.max(np.abs(alt - want)) < 1e-14
+
+
+def pin_bruteforce():
+    r = _rng(11)
+    for N, d, scale in ((1, 3, 1.0), (2, 4, 1.0), (7, 16, 3.0), (64, 8, 10.0), (200, 5, 30.0)):
+        q = r.standard_normal(d).astype(np.float32)
+        K = (scale * r.standard_normal((N, d))).astype(np.float32)
+        V = r.standard_normal((N, d)).astype(np.float32)
+        O, m, u, w = oracle.scan(q, K, V)
+        s = oracle.scores(q, K)
+        Ob = oracle.bruteforce(s, V)
+        assert _rel(O, Ob) < 1e-12, (N, d, _rel(O, Ob))
+
+
+def pin_last_row():
+    r = _rng(12)
+    for N, d in ((1, 4), (33, 16), (300, 64)):
+        q = r.standard_normal(d).astype(np.float32)
+        K = (2 * r.standard_normal((N, d))).astype(np.float32)
+        V = r.standard_normal((N, d)).astype(np.float32)
+        O, m, u, w = oracle.scan(q, K, V)
+        s_np = K.astype(np.float64) @ q.astype(np.float64)
+        ref = scipy.special.softmax(s_np) @ V.astype(np.float64)
+        assert _rel(O[-1], ref) < 1e-12
+        assert abs(m - s_np.max()) <= 1e-12 * max(1.0, abs(s_np.max()))
+        assert abs(w - np.exp(s_np - s_np.max()).sum()) < 1e-10 * N
+        assert _rel(u / w, ref) < 1e-12
+
+
+def pin_scores():
+    r = _rng(13)
+    q = r.standard_normal(64).astype(np.float32)
+    K = r.standard_normal((100, 64)).astype(np.float32)
+    s = oracle.scores(q, K)
+    ref = K.astype(np.float64) @ q.astype(np.float64)
+    assert np.max(np.abs(s - ref)) < 1e-12
+
+
+def pin_shift():
+    r = _rng(14)
+    N, d = 150, 8
+    s = 5 * r.standard_normal(N)
+    V = r.standard_normal((N, d)).astype(np.float32)
+    O0, m0, u0, w0 = oracle.scan_scores(s, V)
+    for c in (100.0, -700.0, 0.5):
+        O1, m1, u1, w1 = oracle.scan_scores(s + c, V)
+        assert _rel(O1, O0) < 1e-12
+        assert abs(m1 - (m0 + c)) < 1e-9
+        assert abs(w1 - w0) < 1e-12 * w0
+        assert _rel(u1, u0) < 1e-12
+
+
+def pin_equal_scores():
+    r = _rng(15)
+    for N, d in ((1, 4), (97, 16)):
+        q = np.zeros(d, dtype=np.float32)
+        K = r.standard_normal((N, d)).astype(np.float32)
+        V = r.standard_normal((N, d)).astype(np.float32)
+        O, m, u, w = oracle.scan(q, K, V)
+        ref = np.cumsum(V.astype(np.float64), axis=0) / np.arange(1, N + 1)[:, None]
+        assert _rel(O, ref) < 1e-12
+        assert m == 0.0 and abs(w - N) < 1e-9
+
+
+def pin_hillis_steele():
+    r = _rng(16)
+    for N, d in ((1, 2), (2, 3), (3, 4), (100, 8), (257, 5), (64, 16)):
+        s = 20 * r.standard_normal(N)
+        V = r.standard_normal((N, d)).astype(np.float32)
+        O, m, u, w = oracle.scan_scores(s, V)
+        Oh = oracle.hillis_steele(s, V)
+        assert _rel(Oh, O) < 1e-12, (N, d)
+
+
+def _state(r, d, m=None):
+    m = float(10 * r.standard_normal()) if m is None else m
+    return m, r.standard_normal(d), float(abs(r.standard_normal()) + 0.1)
+
+
+def _same_state(a, b, tol=1e-12):
+    # compare as functions of the represented sums: rebase b to a's m
+    ma, ua, wa = a
+    mb, ub, wb = b
+    if ma == -np.inf or mb == -np.inf:
+        return ma == mb and wa == wb == 0.0 and not np.any(ua) and not np.any(ub)
+    f = np.exp(mb - ma)
+    return (abs(ma - mb) < 1e-12 * max(1.0, abs(ma))
+            and abs(wb * f - wa) <= tol * abs(wa)
+            and np.max(np.abs(ub * f - ua)) <= tol * max(1e-300, np.max(np.abs(ua))))
+
+
+def pin_operator_laws():
+    r = _rng(17)
+    d = 6
+    ident = (-np.inf, np.zeros(d), 0.0)
+    for _ in range(50):
+        a, b, c = _state(r, d), _state(r, d), _state(r, d)
+        ab_c = oracle.combine(oracle.combine(a, b), c)
+        a_bc = oracle.combine(a, oracle.combine(b, c))
+        assert _same_state(ab_c, a_bc)
+        assert _same_state(oracle.combine(a, b), oracle.combine(b, a))
+        assert _same_state(oracle.combine(ident, a), a)
+        assert _same_state(oracle.combine(a, ident), a)
+    assert _same_state(oracle.combine(ident, ident), ident)
+    # the operator on two leaves equals the two-token softmax (closed form)
+    v1, v2 = r.standard_normal(d), r.standard_normal(d)
+    m, u, w = oracle.combine((1.5, v1, 1.0), (-0.5, v2, 1.0))
+    p = 1.0 / (1.0 + np.exp(-2.0))
+    assert m == 1.5 and np.max(np.abs(u / w - (p * v1 + (1 - p) * v2))) < 1e-14
+
+
+def pin_first_output():
+    r = _rng(18)
+    for d in (1, 16, 128):
+        q = r.standard_normal(d).astype(np.float32)
+        K = r.standard_normal((5, d)).astype(np.float32)
+        V = r.standard_normal((5, d)).astype(np.float32)
+        O, m, u, w = oracle.scan(q, K, V)
+        assert np.array_equal(O[0], V[0].astype(np.float64))
+
+
+def pin_one_hot():
+    r = _rng(19)
+    N, d, star = 64, 8, 20
+    s = r.standard_normal(N)
+    s[star] = s.max() + 60.0
+    V = r.standard_normal((N, d)).astype(np.float32)
+    O, m, u, w = oracle.scan_scores(s, V)
+    assert np.max(np.abs(O[star:] - V[star].astype(np.float64))) < N * np.exp(-55)
+    assert _rel(O[:star], oracle.bruteforce(s[:star], V[:star])) < 1e-12
+
+
+def pin_bounds():
+    r = _rng(20)
+    N, d = 120, 8
+    s = 15 * r.standard_normal(N)
+    V = r.standard_normal((N, d)).astype(np.float32)
+    O, m, u, w = oracle.scan_scores(s, V)
+    Vd = V.astype(np.float64)
+    lo = np.minimum.accumulate(Vd, axis=0)
+    hi = np.maximum.accumulate(Vd, axis=0)
+    assert np.all(O >= lo - 1e-12) and np.all(O <= hi + 1e-12)
+    assert m == s.max()
+    assert 1.0 <= w <= N
+    for t in (1, 2, 10, 57):   # the prefix states obey the same bounds
+        _, mt, ut, wt = oracle.scan_scores(s[:t], V[:t], want_O=False)
+        assert mt == s[:t].max() and 1.0 <= wt <= t
+
+
+def pin_long_double():
+    r = _rng(21)
+    q = r.standard_normal(16).astype(np.float32)
+    K = (4 * r.standard_normal((256, 16))).astype(np.float32)
+    V = r.standard_normal((256, 16)).astype(np.float32)
+    O, m, u, w = oracle.scan(q, K, V)
+    Ol, ml, ul, wl = oracle.scan_longdouble(q, K, V)
+    assert _rel(O, Ol) < 1e-13
+    assert abs(m - ml) < 1e-13 * max(1.0, abs(ml))
+    assert abs(w - wl) < 1e-13 * wl and _rel(u, ul) < 1e-13
+
+
+def pin_large_scores():
+    r = _rng(22)
+    N, d = 90, 4
+    s = 2000 * r.standard_normal(N)
+    s[::7] = 5000.0 - r.random(len(s[::7]))
+    V = r.uniform(-1, 1, (N, d)).astype(np.float32)
+    O, m, u, w = oracle.scan_scores(s, V)
+    assert np.all(np.isfinite(O)) and np.isfinite(w) and np.all(np.isfinite(u))
+    assert _rel(O, oracle.bruteforce(s, V)) < 1e-12
+
+
+def pin_continuation():
+    r = _rng(23)
+    N, d = 200, 8
+    q = r.standard_normal(d).astype(np.float32)
+    K = (3 * r.standard_normal((N, d))).astype(np.float32)
+    V = r.standard_normal((N, d)).astype(np.float32)
+    O, m, u, w = oracle.scan(q, K, V)
+    for cut in (1, 50, 199):
+        _, ma, ua, wa = oracle.scan(q, K[:cut], V[:cut], want_O=False)
+        Ob, mb, ub, wb = oracle.scan(q, K[cut:], V[cut:], init=(ma, ua, wa))
+        assert _rel(Ob, O[cut:]) < 1e-12
+        assert _same_state((m, u, w), (mb, ub, wb))
+
+
+def pin_running_sum():
+    # the memory-efficient-attention review's section 2 algorithm taken as
+    # written: unscaled sums v* += v e^s, s* += e^s, output v*/s* (scores kept
+    # moderate so e^s cannot overflow)
+    r = _rng(24)
+    N, d = 80, 6
+    s = 3 * r.standard_normal(N)
+    V = r.standard_normal((N, d)).astype(np.float32)
+    vstar = np.zeros(d)
+    sstar = 0.0
+    ref = np.empty((N, d))
+    for t in range(N):
+        vstar = vstar + V[t].astype(np.float64) * np.exp(s[t])
+        sstar = sstar + np.exp(s[t])
+        ref[t] = vstar / sstar
+    O, m, u, w = oracle.scan_scores(s, V)
+    assert _rel(O, ref) < 1e-12
+
+
+ALL_PINS = [
+    pin_worked_example, pin_bruteforce, pin_last_row, pin_scores, pin_shift,
+    pin_equal_scores, pin_hillis_steele, pin_operator_laws, pin_first_output,
+    pin_one_hot, pin_bounds, pin_long_double, pin_large_scores, pin_continuation,
+    pin_running_sum,
+]
