@@ -10,10 +10,7 @@ __all__ = ["binding", "inputs"]
 
 
 def __getattr__(name):
-    if name == "binding":
-        from . import binding
-        return binding
-    if name == "inputs":
-        from . import inputs
-        return inputs
+    if name in __all__:
+        import importlib
+        return importlib.import_module(f"{__name__}.{name}")
     raise AttributeError(name)
