@@ -1,0 +1,371 @@
+// aaren_api.cu -- host side of libaaren: argument checks, tile selection,
+// workspace layout, launches and the device status word.  The operation and
+// the conventions are documented in include/aaren.h.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <climits>
+#include <cstdint>
+#include <cstdlib>
+
+#include "aaren.h"
+#include "common.cuh"
+#include "scan_kernel.cuh"
+#include "step_kernel.cuh"
+
+namespace aaren {
+
+// Per-device status word; kernels OR failure bits into it, aaren_check reads
+// and clears it.
+__device__ unsigned g_status;
+
+namespace {
+
+constexpr int64_t kDefaultWaitLimitNs = 1000000000;   // 1 s
+std::atomic<int64_t> g_fault_chunk{-1};
+std::atomic<int64_t> g_wait_limit_ns{kDefaultWaitLimitNs};
+
+constexpr size_t kHeaderBytes = 256;   // ticket counter, padded
+
+bool supported_d(int64_t d) { return d == 16 || d == 32 || d == 64 || d == 128; }
+bool supported_dtype(int32_t t) { return t == AAREN_F32 || t == AAREN_BF16 || t == AAREN_BF16_F32OUT; }
+
+size_t in_elem_bytes(int32_t dtype) { return dtype == AAREN_F32 ? 4 : 2; }
+size_t out_elem_bytes(int32_t dtype) { return dtype == AAREN_BF16 ? 2 : 4; }
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// a * b without int64 overflow (a, b >= 0)
+bool mul_ok(int64_t a, int64_t b, int64_t *out)
+{
+    if (a != 0 && b > INT64_MAX / a) return false;
+    *out = a * b;
+    return true;
+}
+
+// Tile shape per (d, input type): warps per block and 32-token groups per
+// warp; a chunk is warps * groups * 32 tokens.  Chosen so K and V of one
+// chunk fill about 64 KB of shared memory (3 blocks per SM).
+template <int D, typename Tin>
+struct TileChoice {
+    static constexpr int WARPS = (sizeof(Tin) == 4 && D == 128) ? 2 : 4;
+    static constexpr int GROUPS = 1;
+    static constexpr int C = WARPS * GROUPS * 32;
+};
+
+int64_t chunk_tokens(int64_t d, int32_t dtype)
+{
+    const bool f32 = (dtype == AAREN_F32);
+    switch (d) {
+    case 16: return f32 ? TileChoice<16, float>::C : TileChoice<16, __nv_bfloat16>::C;
+    case 32: return f32 ? TileChoice<32, float>::C : TileChoice<32, __nv_bfloat16>::C;
+    case 64: return f32 ? TileChoice<64, float>::C : TileChoice<64, __nv_bfloat16>::C;
+    case 128: return f32 ? TileChoice<128, float>::C : TileChoice<128, __nv_bfloat16>::C;
+    default: return 0;
+    }
+}
+
+struct WorkspaceLayout {
+    size_t flags_off, states_off, bytes, zero_bytes;
+    int64_t chunks_per_head, total_chunks;
+};
+
+// Workspace: [ticket | pad to 256] [flags: u32 per chunk, padded to 256]
+// [states: per chunk 2 x (d + 4) floats].  Only the ticket and the flags need
+// zeroing before a launch (zero_bytes).
+bool workspace_layout(int64_t BH, int64_t N, int64_t d, int64_t C, WorkspaceLayout *w)
+{
+    if (C <= 0) return false;
+    const int64_t cph = (N + C - 1) / C;
+    int64_t total;
+    if (!mul_ok(BH, cph, &total)) return false;
+    if (total > INT_MAX) return false;   // one block per chunk, 32-bit ticket
+    w->chunks_per_head = cph;
+    w->total_chunks = total;
+    const size_t flag_bytes = ((size_t(total) * 4 + 255) / 256) * 256;
+    w->flags_off = kHeaderBytes;
+    w->states_off = kHeaderBytes + flag_bytes;
+    w->zero_bytes = kHeaderBytes + flag_bytes;
+    w->bytes = w->states_off + size_t(total) * 2 * size_t(d + 4) * sizeof(float);
+    return true;
+}
+
+template <typename Kernel>
+cudaError_t allow_smem(Kernel kern, size_t bytes, std::atomic<unsigned long long> &done)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long bit = 1ull << (dev & 63);
+    if (done.load() & bit) return cudaSuccess;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(bytes));
+    if (e == cudaSuccess) done.fetch_or(bit);
+    return e;
+}
+
+template <int D, typename Tin, typename Tout>
+aaren_status_t launch_scan(const ScanParams &p, int64_t total_chunks, cudaStream_t st)
+{
+    using TC = TileChoice<D, Tin>;
+    using Tile = ScanTile<D, Tin, TC::WARPS, TC::GROUPS>;
+    static std::atomic<unsigned long long> configured{0};
+    auto kern = k_scan_fwd<D, Tin, Tout, TC::WARPS, TC::GROUPS>;
+    if (allow_smem(kern, Tile::smem_bytes, configured) != cudaSuccess) return AAREN_ERR_CUDA;
+    kern<<<unsigned(total_chunks), TC::WARPS * 32, Tile::smem_bytes, st>>>(p);
+    return cudaGetLastError() == cudaSuccess ? AAREN_OK : AAREN_ERR_CUDA;
+}
+
+template <int D>
+aaren_status_t dispatch_scan_dtype(const ScanParams &p, int64_t total, int32_t dtype,
+                                   cudaStream_t st)
+{
+    switch (dtype) {
+    case AAREN_F32: return launch_scan<D, float, float>(p, total, st);
+    case AAREN_BF16: return launch_scan<D, __nv_bfloat16, __nv_bfloat16>(p, total, st);
+    case AAREN_BF16_F32OUT: return launch_scan<D, __nv_bfloat16, float>(p, total, st);
+    default: return AAREN_ERR_UNSUPPORTED;
+    }
+}
+
+aaren_status_t dispatch_scan(const ScanParams &p, int64_t total, int64_t d, int32_t dtype,
+                             cudaStream_t st)
+{
+    switch (d) {
+    case 16: return dispatch_scan_dtype<16>(p, total, dtype, st);
+    case 32: return dispatch_scan_dtype<32>(p, total, dtype, st);
+    case 64: return dispatch_scan_dtype<64>(p, total, dtype, st);
+    case 128: return dispatch_scan_dtype<128>(p, total, dtype, st);
+    default: return AAREN_ERR_UNSUPPORTED;
+    }
+}
+
+template <int D, typename Tin, typename Tout>
+aaren_status_t launch_step(const StepParams &p, cudaStream_t st)
+{
+    const int64_t threads = p.n * 32;
+    const unsigned blocks = unsigned((threads + 255) / 256);
+    k_step<D, Tin, Tout><<<blocks, 256, 0, st>>>(p);
+    return cudaGetLastError() == cudaSuccess ? AAREN_OK : AAREN_ERR_CUDA;
+}
+
+template <int D>
+aaren_status_t dispatch_step_dtype(const StepParams &p, int32_t dtype, cudaStream_t st)
+{
+    switch (dtype) {
+    case AAREN_F32: return launch_step<D, float, float>(p, st);
+    case AAREN_BF16: return launch_step<D, __nv_bfloat16, __nv_bfloat16>(p, st);
+    case AAREN_BF16_F32OUT: return launch_step<D, __nv_bfloat16, float>(p, st);
+    default: return AAREN_ERR_UNSUPPORTED;
+    }
+}
+
+aaren_status_t launch_state_init(float *m, float *u, float *w, int64_t n, int64_t d,
+                                 cudaStream_t st)
+{
+    const int64_t total = n * d;
+    int64_t blocks = (total + 255) / 256;
+    if (blocks > 4096) blocks = 4096;
+    k_state_init<<<unsigned(blocks), 256, 0, st>>>(m, u, w, n, d);
+    return cudaGetLastError() == cudaSuccess ? AAREN_OK : AAREN_ERR_CUDA;
+}
+
+bool overlaps(const void *a, size_t abytes, const void *b, size_t bbytes)
+{
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    return a0 < b0 + bbytes && b0 < a0 + abytes;
+}
+
+// The state triple must be all NULL or all set; u 16-byte, m and w 4-byte aligned.
+aaren_status_t check_state(const float *m, const float *u, const float *w)
+{
+    const int set = (m != nullptr) + (u != nullptr) + (w != nullptr);
+    if (set != 0 && set != 3) return AAREN_ERR_INVALID;
+    if (set == 3 && (!aligned(u, 16) || !aligned(m, 4) || !aligned(w, 4))) return AAREN_ERR_INVALID;
+    return AAREN_OK;
+}
+
+}  // namespace
+}  // namespace aaren
+
+using namespace aaren;
+
+extern "C" {
+
+size_t aaren_scan_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t d)
+{
+    if (!supported_d(d) || B < 0 || H < 0 || N < 0) return SIZE_MAX;
+    int64_t BH;
+    if (!mul_ok(B, H, &BH)) return SIZE_MAX;
+    if (BH == 0 || N == 0) return 0;
+    // the workspace depends on the chunk, which depends on the dtype only for
+    // float32 d = 128; take the smaller chunk so the size covers every dtype
+    int64_t C = chunk_tokens(d, AAREN_F32);
+    const int64_t Cb = chunk_tokens(d, AAREN_BF16);
+    if (Cb < C) C = Cb;
+    WorkspaceLayout w;
+    if (!workspace_layout(BH, N, d, C, &w)) return SIZE_MAX;
+    return w.bytes;
+}
+
+aaren_status_t aaren_scan_forward_ex(const void *q, const void *K, const void *V, void *O,
+                                     int64_t B, int64_t H, int64_t N, int64_t d, int32_t dtype,
+                                     const float *m_in, const float *u_in, const float *w_in,
+                                     float *m_out, float *u_out, float *w_out, void *workspace,
+                                     size_t workspace_bytes, void *stream)
+{
+    if (!supported_dtype(dtype) || !supported_d(d)) return AAREN_ERR_UNSUPPORTED;
+    if (B < 0 || H < 0 || N < 0) return AAREN_ERR_INVALID;
+    if (check_state(m_in, u_in, w_in) != AAREN_OK) return AAREN_ERR_INVALID;
+    if (check_state(m_out, u_out, w_out) != AAREN_OK) return AAREN_ERR_INVALID;
+    int64_t BH, BHN, elems;
+    if (!mul_ok(B, H, &BH) || !mul_ok(BH, N, &BHN) || !mul_ok(BHN, d, &elems)) return AAREN_ERR_INVALID;
+    int64_t kv_bytes, o_bytes;
+    if (!mul_ok(elems, int64_t(in_elem_bytes(dtype)), &kv_bytes) ||
+        !mul_ok(elems, int64_t(out_elem_bytes(dtype)), &o_bytes))
+        return AAREN_ERR_INVALID;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (BH == 0) return AAREN_OK;
+    if (N == 0) {
+        // final state = starting state
+        if (m_out == nullptr) return AAREN_OK;
+        if (m_in == nullptr) return launch_state_init(m_out, u_out, w_out, BH, d, st);
+        if (cudaMemcpyAsync(m_out, m_in, size_t(BH) * 4, cudaMemcpyDeviceToDevice, st) != cudaSuccess ||
+            cudaMemcpyAsync(w_out, w_in, size_t(BH) * 4, cudaMemcpyDeviceToDevice, st) != cudaSuccess ||
+            cudaMemcpyAsync(u_out, u_in, size_t(BH) * d * 4, cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+            return AAREN_ERR_CUDA;
+        return AAREN_OK;
+    }
+    if (q == nullptr || K == nullptr || V == nullptr || O == nullptr) return AAREN_ERR_INVALID;
+    if (!aligned(q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(O, 16)) return AAREN_ERR_INVALID;
+    if (overlaps(O, size_t(o_bytes), K, size_t(kv_bytes)) || overlaps(O, size_t(o_bytes), V, size_t(kv_bytes)))
+        return AAREN_ERR_INVALID;
+
+    const int64_t C = chunk_tokens(d, dtype);
+    WorkspaceLayout wl;
+    if (!workspace_layout(BH, N, d, C, &wl)) return AAREN_ERR_INVALID;
+
+    void *ws = workspace;
+    bool owned = false;
+    if (ws == nullptr) {
+        if (cudaMallocAsync(&ws, wl.bytes, st) != cudaSuccess) return AAREN_ERR_CUDA;
+        owned = true;
+    } else if (workspace_bytes < wl.bytes || !aligned(ws, 256)) {
+        return AAREN_ERR_WORKSPACE;
+    }
+    aaren_status_t rc = AAREN_OK;
+    if (cudaMemsetAsync(ws, 0, wl.zero_bytes, st) != cudaSuccess) {
+        rc = AAREN_ERR_CUDA;
+    } else {
+        unsigned *status = nullptr;
+        if (cudaGetSymbolAddress(reinterpret_cast<void **>(&status), g_status) != cudaSuccess) {
+            rc = AAREN_ERR_CUDA;
+        } else {
+            char *base = static_cast<char *>(ws);
+            ScanParams p;
+            p.q = q; p.K = K; p.V = V; p.O = O;
+            p.m_in = m_in; p.u_in = u_in; p.w_in = w_in;
+            p.m_out = m_out; p.u_out = u_out; p.w_out = w_out;
+            p.ticket = reinterpret_cast<unsigned *>(base);
+            p.flags = reinterpret_cast<unsigned *>(base + wl.flags_off);
+            p.states = reinterpret_cast<float *>(base + wl.states_off);
+            p.status = status;
+            p.N = N;
+            p.chunks_per_head = wl.chunks_per_head;
+            p.fault_chunk = g_fault_chunk.load();
+            p.wait_limit_ns = g_wait_limit_ns.load();
+            rc = dispatch_scan(p, wl.total_chunks, d, dtype, st);
+        }
+    }
+    if (owned && cudaFreeAsync(ws, st) != cudaSuccess && rc == AAREN_OK) rc = AAREN_ERR_CUDA;
+    return rc;
+}
+
+aaren_status_t aaren_scan_forward(const void *q, const void *K, const void *V, void *O, int64_t B,
+                                  int64_t H, int64_t N, int64_t d, int32_t dtype, void *stream)
+{
+    return aaren_scan_forward_ex(q, K, V, O, B, H, N, d, dtype, nullptr, nullptr, nullptr, nullptr,
+                                 nullptr, nullptr, nullptr, 0, stream);
+}
+
+aaren_status_t aaren_state_init(float *m, float *u, float *w, int64_t n, int64_t d, void *stream)
+{
+    if (!supported_d(d)) return AAREN_ERR_UNSUPPORTED;
+    if (n < 0) return AAREN_ERR_INVALID;
+    int64_t nd;
+    if (!mul_ok(n, d, &nd)) return AAREN_ERR_INVALID;
+    if (n == 0) return AAREN_OK;
+    if (m == nullptr || u == nullptr || w == nullptr) return AAREN_ERR_INVALID;
+    if (check_state(m, u, w) != AAREN_OK) return AAREN_ERR_INVALID;
+    return launch_state_init(m, u, w, n, d, static_cast<cudaStream_t>(stream));
+}
+
+aaren_status_t aaren_step(const void *q, float *m, float *u, float *w, const void *k_t,
+                          const void *v_t, void *o_t, int64_t n, int64_t d, int32_t dtype,
+                          void *stream)
+{
+    if (!supported_dtype(dtype) || !supported_d(d)) return AAREN_ERR_UNSUPPORTED;
+    if (n < 0) return AAREN_ERR_INVALID;
+    int64_t nd, threads;
+    if (!mul_ok(n, d, &nd) || !mul_ok(n, 32, &threads) || threads / 256 >= INT_MAX) return AAREN_ERR_INVALID;
+    if (n == 0) return AAREN_OK;
+    if (q == nullptr || k_t == nullptr || v_t == nullptr || o_t == nullptr || m == nullptr ||
+        u == nullptr || w == nullptr)
+        return AAREN_ERR_INVALID;
+    if (!aligned(q, 16) || !aligned(k_t, 16) || !aligned(v_t, 16) || !aligned(o_t, 16))
+        return AAREN_ERR_INVALID;
+    if (check_state(m, u, w) != AAREN_OK) return AAREN_ERR_INVALID;
+    StepParams p;
+    p.q = q; p.m = m; p.u = u; p.w = w; p.k = k_t; p.v = v_t; p.o = o_t; p.n = n;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    switch (d) {
+    case 16: return dispatch_step_dtype<16>(p, dtype, st);
+    case 32: return dispatch_step_dtype<32>(p, dtype, st);
+    case 64: return dispatch_step_dtype<64>(p, dtype, st);
+    case 128: return dispatch_step_dtype<128>(p, dtype, st);
+    default: return AAREN_ERR_UNSUPPORTED;
+    }
+}
+
+aaren_status_t aaren_check(void *stream)
+{
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return AAREN_ERR_CUDA;
+    unsigned bits = 0;
+    if (cudaMemcpyFromSymbol(&bits, g_status, sizeof(bits)) != cudaSuccess) return AAREN_ERR_CUDA;
+    if (bits == 0) return AAREN_OK;
+    const unsigned zero = 0;
+    if (cudaMemcpyToSymbol(g_status, &zero, sizeof(zero)) != cudaSuccess) return AAREN_ERR_CUDA;
+    if (bits & STATUS_LOAD_TIMEOUT) return AAREN_ERR_LOAD_TIMEOUT;
+    return AAREN_ERR_LOOKBACK_TIMEOUT;
+}
+
+const char *aaren_status_string(int32_t status)
+{
+    switch (status) {
+    case AAREN_OK: return "ok";
+    case AAREN_ERR_INVALID: return "invalid argument";
+    case AAREN_ERR_UNSUPPORTED: return "unsupported d or dtype";
+    case AAREN_ERR_CUDA: return "CUDA runtime error";
+    case AAREN_ERR_LOOKBACK_TIMEOUT: return "device: cross-block carry wait gave up";
+    case AAREN_ERR_LOAD_TIMEOUT: return "device: bulk copy into shared memory did not complete";
+    case AAREN_ERR_WORKSPACE: return "workspace too small or misaligned";
+    default: return "unknown status";
+    }
+}
+
+int32_t aaren_abi_version(void) { return 1; }
+
+aaren_status_t aaren_debug_set_fault(int64_t never_publish_chunk, int64_t wait_limit_ns)
+{
+    g_fault_chunk.store(never_publish_chunk < 0 ? -1 : never_publish_chunk);
+    g_wait_limit_ns.store(wait_limit_ns <= 0 ? kDefaultWaitLimitNs : wait_limit_ns);
+    return AAREN_OK;
+}
+
+int64_t aaren_scan_chunk_tokens(int64_t d, int32_t dtype)
+{
+    if (!supported_d(d) || !supported_dtype(dtype)) return 0;
+    return chunk_tokens(d, dtype);
+}
+
+}  // extern "C"

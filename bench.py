@@ -1,0 +1,401 @@
+#!/usr/bin/env python3
+"""Benchmark of the softmax-attention prefix scan on one or more B300 GPUs.
+
+One step = one aaren_scan_forward over the whole workload (scores, chunk
+scan, cross-chunk carry, output), inputs resident in HBM.  The default
+workload is the long sequence: B=1, H=16, N=2^20 tokens, d=128, q/K/V
+bfloat16 ~ N(0,1) (seed 3), bfloat16 output, float32 arithmetic.  Its inputs
+(8.6 GB of K and V) are far larger than L2 (126 MB), so no L2 flush is needed
+between steps.
+
+Prints ONE JSON line (rank 0):
+  value      head-tokens/s (B*H*N per step / mean step time, all ranks)
+  roofline   HBM roofline of the scan kernel: algorithmic bytes (K and V read
+             once, O written once) per launch / mean launch time, against the
+             measured HBM copy peak
+  e2e        the same metric through the C ABI with host buffers: per step
+             host->device copy of q, K, V from pinned memory, the scan, and the
+             device->host copy of O
+  cpu_baseline  the float64 oracle timed on this host's cores on a bounded
+             sample of the same workload
+With torchrun (N > 1) every rank runs its own copy of the workload (heads are
+independent: no collective on the data path), the step time is the maximum
+over ranks and value counts the head-tokens of all ranks (weak scaling).
+
+`--impl reference` times the float64 oracle instead (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+FALLBACK_HBM_GBS = 6400.0
+CPU_SAMPLE_TOKENS = 1 << 18      # per head, cpu_baseline leg
+REF_STEP_TOKENS = 1 << 16        # per head, --impl reference steps
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="long", choices=["tiny", "bf16_4k", "stress", "long"])
+    ap.add_argument("--heads", type=int, default=0, help="override H (profiling small cases)")
+    ap.add_argument("--out-dtype", default="", choices=["", "bf16", "f32"])
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def workload(args):
+    from attention_prefix_scan_02_b300 import inputs
+    wl = inputs.WORKLOADS[args.workload]
+    if args.heads:
+        wl = inputs.custom(wl.B, args.heads, wl.N, wl.d, wl.dtype, wl.seed, wl.kind, wl.name)
+    return wl
+
+
+def describe(wl, out):
+    recipe = {"normal": "q, K, V ~ N(0,1)",
+              "stress": "q ~ N(0,1), K ~ 8 N(0,1), every 97th key = 3q, V ~ U(-1,1)",
+              "stream": "per-head q shared by streams, K, V ~ N(0,1)"}[wl.kind]
+    return {"workload": f"{wl.name}: B={wl.B} H={wl.H} N={wl.N} d={wl.d}, {wl.dtype} in, {out} out, "
+                        f"{recipe}, seed {wl.seed}",
+            "B": wl.B, "H": wl.H, "N": wl.N, "d": wl.d, "in_dtype": wl.dtype, "out_dtype": out,
+            "l2": "no flush: K+V per step far larger than the 126 MB L2" if wl.N * wl.d * wl.heads >= (1 << 26)
+            else "L2 flushed (write of 2x L2 size) before every timed step"}
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "attention_prefix_scan_02_b300", "csrc")
+    for fn in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, fn), "rb") as f:
+            h.update(fn.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(wl, out):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source for this workload; else None."""
+    path = os.path.join(ROOT, "profiles", "scan_long_bf16_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if rec.get("kernel_source_sha") != kernel_source_hash():
+        return None
+    if rec.get("workload") != wl.name or rec.get("out_dtype") != out:
+        return None
+    per_head = rec.get("dram_bytes_per_head")
+    return None if per_head is None else int(per_head * wl.heads)
+
+
+def measured_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            mp = json.load(f)
+        return float(mp["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs, copy read+write)"
+    except (OSError, ValueError, KeyError):
+        return FALLBACK_HBM_GBS, "fallback (6.4 TB/s, earlier B300 measurement)"
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(prefix="clocks", suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or self.path is None:
+            return None
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+                except ValueError:
+                    continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r) if v == "Active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+def cpu_oracle_rate(wl, tokens_per_head, threads):
+    """Time the float64 oracle (as it stands) over `tokens_per_head` leading
+    tokens of every head, heads spread over `threads` host threads.  Inputs
+    are drawn before the clock starts.  Returns (head-tokens/s, seconds)."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    import oracle
+    from attention_prefix_scan_02_b300 import inputs
+    n = min(tokens_per_head, wl.N)
+    sub = inputs.custom(wl.B, wl.H, n, wl.d, wl.dtype, wl.seed, wl.kind, wl.name)
+    heads = [inputs.head_inputs(sub, b, h) for b in range(wl.B) for h in range(wl.H)]
+
+    def one(x):
+        q, K, V = x
+        oracle.scan(q, K, V)      # O is computed and discarded
+
+    t0 = time.perf_counter()
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        list(ex.map(one, heads))
+    dt = time.perf_counter() - t0
+    return len(heads) * n / dt, dt, n
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    wl = workload(args)
+    out = args.out_dtype or wl.dtype
+    cores = host_cores()
+    threads = min(cores, wl.heads)
+    rates = []
+    for i in range(args.warmup + args.steps):
+        r, dt, n = cpu_oracle_rate(wl, REF_STEP_TOKENS, threads)
+        if i >= args.warmup:
+            rates.append((r, dt))
+    n = min(REF_STEP_TOKENS, wl.N)
+    sample = f"each step: the first {n} tokens of all {wl.heads} heads ({n * wl.heads} head-tokens)"
+    value = statistics.mean(r for r, _ in rates)
+    line = {"impl": "reference", "metric": "head-tokens/s of the Aaren prefix scan (and HBM GB/s)",
+            "value": value, "unit": "head-tokens/s", "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * statistics.mean(dt for _, dt in rates),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": describe(wl, out),
+            "cpu_baseline": {"value": value, "unit": "head-tokens/s", "cores": threads,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "head-tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    import torch
+
+    rank, world, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (the library has no CPU path)")
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    from attention_prefix_scan_02_b300 import binding, build, inputs
+    build.build()
+    wl = workload(args)
+    out = args.out_dtype or wl.dtype
+    out_t = torch.bfloat16 if out == "bf16" else torch.float32
+    in_t = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
+    warmup = max(3, args.warmup)
+
+    # CPU baseline first (host memory is freed before the GPU legs)
+    cpu = None
+    if rank == 0:
+        cores = host_cores()
+        threads = min(cores, wl.heads)
+        rate, dt, n = cpu_oracle_rate(wl, CPU_SAMPLE_TOKENS, threads)
+        cpu = {"value": rate, "unit": "head-tokens/s", "cores": threads, "kind": "oracle",
+               "sample": f"the first {n} tokens of all {wl.heads} heads ({n * wl.heads} head-tokens, "
+                         f"{dt:.1f} s wall on {threads} threads)"}
+
+    q, K, V = inputs.batch_inputs(wl, device="cuda")
+    O = torch.empty(K.shape, dtype=out_t, device="cuda")
+    ws = binding.new_workspace(wl.B, wl.H, wl.N, wl.d)
+    stream = torch.cuda.current_stream()
+    in_b = 2 if wl.dtype == "bf16" else 4
+    out_b = 2 if out == "bf16" else 4
+    elems = wl.heads * wl.N * wl.d
+    alg_bytes = elems * (2 * in_b + out_b)          # K, V read once + O written once
+    tokens = wl.heads * wl.N
+    flush = None
+    if elems * 2 * in_b < (1 << 28):                # small workloads sit in L2: flush it
+        flush = torch.empty(2 * torch.cuda.get_device_properties(0).L2_cache_size // 4 + 1,
+                            dtype=torch.float32, device="cuda")
+
+    def step():
+        binding.aaren_scan_forward_ex(q, K, V, O, workspace=ws, stream=stream)
+
+    for _ in range(warmup):
+        if flush is not None:
+            flush.fill_(1.0)
+        step()
+    if binding.aaren_check() != binding.AAREN_OK:
+        raise SystemExit("device status error during warm-up")
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        time.sleep(0.3)
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        for i in range(args.steps):
+            if flush is not None:
+                flush.fill_(1.0)
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    status = binding.aaren_check()
+    if status != binding.AAREN_OK:
+        raise SystemExit(f"device status error in the timed region: {binding.status_string(status)}")
+    launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    mean_launch_ms = statistics.mean(launch_ms)
+    step_ms = mean_launch_ms if flush is not None else t_start.elapsed_time(t_end) / args.steps
+    if dist is not None:
+        t = torch.tensor([step_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        step_ms = float(t.item())
+
+    # end to end through the C ABI with host buffers
+    e2e = None
+    if rank == 0 or world > 1:
+        hq = torch.empty(q.shape, dtype=in_t, pin_memory=True)
+        hK = torch.empty(K.shape, dtype=in_t, pin_memory=True)
+        hV = torch.empty(V.shape, dtype=in_t, pin_memory=True)
+        hO = torch.empty(O.shape, dtype=out_t, pin_memory=True)
+        hq.copy_(q); hK.copy_(K); hV.copy_(V)
+        dq, dK, dV, dO = q, K, V, O          # device buffers are reused
+        e2e_steps = max(1, min(args.steps, 3))
+
+        def e2e_step():
+            dq.copy_(hq, non_blocking=True)
+            dK.copy_(hK, non_blocking=True)
+            dV.copy_(hV, non_blocking=True)
+            binding.aaren_scan_forward_ex(dq, dK, dV, dO, workspace=ws, stream=stream)
+            hO.copy_(dO, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = a.elapsed_time(b) / e2e_steps
+        if dist is not None:
+            t = torch.tensor([e2e_ms], device="cuda")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        if binding.aaren_check() != binding.AAREN_OK:
+            raise SystemExit("device status error in the end-to-end leg")
+        h2d = (hq.numel() + hK.numel() + hV.numel()) * in_b
+        e2e = {"value": world * tokens / (e2e_ms * 1e-3), "unit": "head-tokens/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": hO.numel() * out_b,
+               "ms_per_step": e2e_ms, "steps": e2e_steps,
+               "path": "pinned host q,K,V -> device, aaren_scan_forward_ex, device O -> pinned host"}
+        del hq, hK, hV, hO
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return 0
+
+    peak, peak_src = measured_peak()
+    achieved = alg_bytes / (mean_launch_ms * 1e-3) / 1e9
+    traffic = profiled_traffic(wl, out)
+    line = {
+        "metric": "head-tokens/s of the Aaren prefix scan (and HBM GB/s)",
+        "value": world * tokens / (step_ms * 1e-3),
+        "unit": "head-tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": warmup, "ms_per_step": step_ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": describe(wl, out),
+        "gpu_launches": args.steps,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "algorithmic_bytes_per_launch": alg_bytes, "launch_ms": mean_launch_ms,
+                     "peak_source": peak_src, "kernel": "k_scan_fwd"},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "clocks": clocks.summary(),
+    }
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

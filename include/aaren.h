@@ -1,0 +1,185 @@
+/*
+ * aaren.h -- C ABI of libaaren, a B300 (sm_103a) CUDA library for the
+ * numerically stable softmax-attention prefix scan.
+ *
+ * The operation.  For every head, given a query q in R^d, keys k_1..k_N and
+ * values v_1..v_N in R^d, the scan produces every causal prefix output
+ *
+ *     s_i = q . k_i                       (unscaled; pre-scale q if wanted)
+ *     o_t = sum_{i<=t} e^{s_i} v_i / sum_{i<=t} e^{s_i},      t = 1..N,
+ *
+ * i.e. attention's many-to-many RNN output computed with a parallel prefix
+ * scan ("Attention as an RNN" review, "Proposed method": attention as a
+ * many-to-one RNN, its many-to-many output via the parallel prefix scan, and
+ * a constant-size state updated one token at a time), which is also the
+ * streaming running sum of the "Self-attention Does Not Need O(n^2) Memory"
+ * review, section 2 "Algorithm" (sums of v_i e^{s_i} and e^{s_i}, divided
+ * at the end), evaluated at every prefix.  The scan carries the state
+ *
+ *     (m, u, w) = (max_i s_i, sum_i e^{s_i - m} v_i, sum_i e^{s_i - m}),
+ *
+ * the max-subtraction reading of that review's section 3 "Numerical
+ * Stability" (whose body the page lacks), combined with the associative
+ * operator (m_a,u_a,w_a) (+) (m_b,u_b,w_b) = (M, e^{m_a-M}u_a + e^{m_b-M}u_b,
+ * e^{m_a-M}w_a + e^{m_b-M}w_b), M = max(m_a, m_b), identity (-inf, 0, 0).
+ * The output is o_t = u_t / w_t of the inclusive prefix state.
+ *
+ * Conventions for every entry point:
+ *  - All tensor pointers are DEVICE pointers owned by the caller; the library
+ *    never frees or keeps them.  Tensors are dense and row-major with the
+ *    last dimension fastest:  q [B,H,d];  K, V, O [B,H,N,d] (each head's
+ *    tokens contiguous, in token order);  state m, w [B*H];  u [B*H, d].
+ *  - q, K, V, O and u pointers must be 16-byte aligned; m, w 4-byte aligned.
+ *  - dtype selects the element types: AAREN_F32 (q, K, V, O float32),
+ *    AAREN_BF16 (q, K, V, O bfloat16), AAREN_BF16_F32OUT (q, K, V bfloat16,
+ *    O float32).  Arithmetic is float32 throughout; bfloat16 inputs are
+ *    widened exactly, bfloat16 outputs are rounded to nearest even.  The state
+ *    (m, u, w) is always float32.
+ *  - d must be 16, 32, 64 or 128 (else AAREN_ERR_UNSUPPORTED).
+ *  - stream is a cudaStream_t (NULL = the legacy default stream).  Every call
+ *    is asynchronous and ordered on that stream.  The return value covers
+ *    argument checks and the launch; failures on the device (a wait that gave
+ *    up) are reported by aaren_check().
+ *  - Non-finite inputs are not checked; NaN and Inf propagate.
+ */
+#ifndef AAREN_H
+#define AAREN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    AAREN_OK = 0,
+    AAREN_ERR_INVALID = 1,          /* bad argument: null or misaligned pointer,
+                                       negative or overflowing size, O aliasing
+                                       K or V, partial state triple */
+    AAREN_ERR_UNSUPPORTED = 2,      /* d or dtype not built */
+    AAREN_ERR_CUDA = 3,             /* a CUDA runtime call failed */
+    AAREN_ERR_LOOKBACK_TIMEOUT = 4, /* device: a cross-block carry wait gave up */
+    AAREN_ERR_LOAD_TIMEOUT = 5,     /* device: a bulk copy into shared memory
+                                       did not complete in time */
+    AAREN_ERR_WORKSPACE = 6         /* caller workspace too small or misaligned */
+} aaren_status_t;
+
+typedef enum {
+    AAREN_F32 = 0,          /* q, K, V, O float32                */
+    AAREN_BF16 = 1,         /* q, K, V, O bfloat16               */
+    AAREN_BF16_F32OUT = 2   /* q, K, V bfloat16, O float32       */
+} aaren_dtype_t;
+
+/*
+ * aaren_scan_forward -- many-to-many output of every head, in one pass over
+ * K and V ("Attention as an RNN" review, "Proposed method": the many-to-many
+ * output by parallel prefix scan).
+ *   q  [B,H,d]     query of each head (dtype's input type)
+ *   K  [B,H,N,d]   keys          V [B,H,N,d] values   (input type)
+ *   O  [B,H,N,d]   output o_t of every prefix, written (output type);
+ *                  must not overlap K or V
+ * N = 0 (or B*H = 0) is a no-op.  The cross-block carry needs a workspace of
+ * aaren_scan_workspace_bytes(B,H,N,d) bytes, taken from the stream-ordered
+ * allocator (cudaMallocAsync / cudaFreeAsync on `stream`) for this call.
+ * Errors: AAREN_ERR_INVALID, AAREN_ERR_UNSUPPORTED, AAREN_ERR_CUDA.
+ */
+aaren_status_t aaren_scan_forward(const void *q, const void *K, const void *V,
+                                  void *O, int64_t B, int64_t H, int64_t N,
+                                  int64_t d, int32_t dtype, void *stream);
+
+/*
+ * aaren_scan_forward_ex -- aaren_scan_forward with an optional starting
+ * state, an optional final state and an optional caller workspace.
+ *   m_in [B*H], u_in [B*H,d], w_in [B*H]   state each head starts from (the
+ *        constant-size RNN state: a stream saved by aaren_step or by an
+ *        earlier scan continues here); all three NULL = the identity
+ *        (-inf, 0, 0).  Read only.
+ *   m_out, u_out, w_out  final state (m, u, w) of each head after token N,
+ *        written; all three NULL = not written.  With N = 0 the final state
+ *        is the starting state.
+ *   workspace, workspace_bytes  device scratch for the cross-block carry, at
+ *        least aaren_scan_workspace_bytes(B,H,N,d) bytes, 256-byte aligned;
+ *        NULL = allocate as aaren_scan_forward does.  Its contents need no
+ *        initialisation and are meaningless after the call.  Two calls in
+ *        flight at once (on different streams) must not share a workspace.
+ * A state triple must be all NULL or all non-NULL (else AAREN_ERR_INVALID).
+ * Errors: as aaren_scan_forward, plus AAREN_ERR_WORKSPACE.
+ */
+aaren_status_t aaren_scan_forward_ex(const void *q, const void *K,
+                                     const void *V, void *O, int64_t B,
+                                     int64_t H, int64_t N, int64_t d,
+                                     int32_t dtype, const float *m_in,
+                                     const float *u_in, const float *w_in,
+                                     float *m_out, float *u_out, float *w_out,
+                                     void *workspace, size_t workspace_bytes,
+                                     void *stream);
+
+/* Bytes of workspace aaren_scan_forward_ex needs for this shape (0 when
+ * N = 0 or B*H = 0; SIZE_MAX when d is unsupported or the shape overflows). */
+size_t aaren_scan_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t d);
+
+/*
+ * aaren_state_init -- set n states to the identity (m = -inf, u = 0, w = 0),
+ * the state of an empty prefix, before the first aaren_step.
+ *   m [n], u [n,d], w [n]   float32, written.
+ * Errors: AAREN_ERR_INVALID, AAREN_ERR_UNSUPPORTED, AAREN_ERR_CUDA.
+ */
+aaren_status_t aaren_state_init(float *m, float *u, float *w, int64_t n,
+                                int64_t d, void *stream);
+
+/*
+ * aaren_step -- one token for each of n independent streams: the constant
+ * memory RNN update of the "Attention as an RNN" review ("Proposed method":
+ * Aaren is updated with new tokens using constant memory):
+ *     s = q . k_t;  M = max(m, s);  u = e^{m-M} u + e^{s-M} v_t;
+ *     w = e^{m-M} w + e^{s-M};  m = M;  o_t = u / w.
+ *   q   [n,d]  query of each stream (input type), read only
+ *   m [n], u [n,d], w [n]  float32 state, read and updated in place
+ *   k_t [n,d], v_t [n,d]   this step's key and value (input type)
+ *   o_t [n,d]  this step's output (output type), written
+ * n = 0 is a no-op.  The states must have been set by aaren_state_init, by
+ * earlier steps, or by aaren_scan_forward_ex's final state.
+ * Errors: AAREN_ERR_INVALID, AAREN_ERR_UNSUPPORTED, AAREN_ERR_CUDA.
+ */
+aaren_status_t aaren_step(const void *q, float *m, float *u, float *w,
+                          const void *k_t, const void *v_t, void *o_t,
+                          int64_t n, int64_t d, int32_t dtype, void *stream);
+
+/*
+ * aaren_check -- synchronise `stream`, then report and clear the device
+ * status word of the current device (one word per device, shared by every
+ * stream and call: a failure on any stream shows up in the next check).
+ * Returns AAREN_OK, AAREN_ERR_LOOKBACK_TIMEOUT, AAREN_ERR_LOAD_TIMEOUT or
+ * AAREN_ERR_CUDA (a CUDA error from the synchronisation).
+ */
+aaren_status_t aaren_check(void *stream);
+
+/* Static, NUL-terminated description of a status code. */
+const char *aaren_status_string(int32_t status);
+
+/* Version of this ABI (incremented on any incompatible change). */
+int32_t aaren_abi_version(void);
+
+/*
+ * aaren_debug_set_fault -- testing hook for the bounded waits.  Every later
+ * scan launch in this process uses these values:
+ *   never_publish_chunk  index (in launch order: head * ceil(N/C) + c) of a
+ *        chunk whose carry is never published, so its successors must give
+ *        up; -1 = none (the default).
+ *   wait_limit_ns        how long a carry wait or a bulk-copy wait lasts
+ *        before it gives up; <= 0 restores the default (1 s).
+ * Returns AAREN_OK.  Not for production use.
+ */
+aaren_status_t aaren_debug_set_fault(int64_t never_publish_chunk,
+                                     int64_t wait_limit_ns);
+
+/* Tokens per chunk (one thread block) the scan uses for this d and dtype
+ * (0 if unsupported); the chunk index of aaren_debug_set_fault counts these. */
+int64_t aaren_scan_chunk_tokens(int64_t d, int32_t dtype);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* AAREN_H */

@@ -1,0 +1,114 @@
+"""The C ABI boundary without a GPU: the library builds and loads, exports
+every function include/aaren.h declares, and its host-only entry points
+(sizes, strings, argument checks that fail before any CUDA call) behave."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from attention_prefix_scan_02_b300 import binding, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "aaren.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^[A-Za-z_][\w \*]*?\b(aaren_\w+)\s*\(", text, flags=re.M)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.load()
+
+
+def test_header_declares_the_abi():
+    names = declared_functions()
+    assert set(names) == set(binding.EXPORTS), names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    raw = ctypes.CDLL(binding.LIB_PATH)
+    for name in declared_functions():
+        assert hasattr(raw, name), name
+
+
+def test_status_strings(lib):
+    for code in range(7):
+        assert binding.status_string(code) and binding.status_string(code) != "unknown status"
+    assert binding.status_string(99) == "unknown status"
+    assert binding.aaren_abi_version() == 1
+
+
+def test_workspace_bytes(lib):
+    assert binding.aaren_scan_workspace_bytes(1, 1, 0, 64) == 0
+    assert binding.aaren_scan_workspace_bytes(0, 4, 100, 64) == 0
+    assert binding.aaren_scan_workspace_bytes(1, 1, 10, 17) == 2 ** 64 - 1
+    n1 = binding.aaren_scan_workspace_bytes(1, 16, 1 << 20, 128)
+    C = min(binding.aaren_scan_chunk_tokens(128, binding.AAREN_F32),
+            binding.aaren_scan_chunk_tokens(128, binding.AAREN_BF16))
+    chunks = 16 * ((1 << 20) // C)
+    assert n1 >= chunks * 2 * (128 + 4) * 4 + chunks * 4
+    # grows with N
+    assert binding.aaren_scan_workspace_bytes(1, 1, 1000, 64) < \
+        binding.aaren_scan_workspace_bytes(1, 1, 100000, 64)
+
+
+def test_chunk_tokens(lib):
+    for d in (16, 32, 64, 128):
+        for dt in (0, 1, 2):
+            c = binding.aaren_scan_chunk_tokens(d, dt)
+            assert c > 0 and c % 32 == 0
+    assert binding.aaren_scan_chunk_tokens(48, 0) == 0
+    assert binding.aaren_scan_chunk_tokens(64, 7) == 0
+
+
+def test_argument_checks_before_any_cuda_call(lib):
+    fake = ctypes.c_void_p(256)   # never dereferenced: each call fails its checks first
+    # unsupported d and dtype
+    assert lib.aaren_scan_forward(fake, fake, fake, fake, 1, 1, 8, 48, 0, None) == binding.AAREN_ERR_UNSUPPORTED
+    assert lib.aaren_scan_forward(fake, fake, fake, fake, 1, 1, 8, 64, 9, None) == binding.AAREN_ERR_UNSUPPORTED
+    # negative sizes, overflow
+    assert lib.aaren_scan_forward(fake, fake, fake, fake, -1, 1, 8, 64, 0, None) == binding.AAREN_ERR_INVALID
+    assert lib.aaren_scan_forward(fake, fake, fake, fake, 1 << 40, 1 << 20, 1 << 20, 64, 0,
+                                  None) == binding.AAREN_ERR_INVALID
+    # null pointers, misalignment, aliasing of O with K
+    assert lib.aaren_scan_forward(None, fake, fake, fake, 1, 1, 8, 64, 0, None) == binding.AAREN_ERR_INVALID
+    assert lib.aaren_scan_forward(fake, ctypes.c_void_p(260), fake, ctypes.c_void_p(1 << 20), 1, 1, 8, 64,
+                                  0, None) == binding.AAREN_ERR_INVALID
+    assert lib.aaren_scan_forward(fake, ctypes.c_void_p(4096), ctypes.c_void_p(1 << 20),
+                                  ctypes.c_void_p(4096 + 256), 1, 1, 8, 64, 0, None) == binding.AAREN_ERR_INVALID
+    # a partial state triple
+    assert lib.aaren_scan_forward_ex(fake, fake, fake, fake, 1, 1, 8, 64, 0, fake, None, None,
+                                     None, None, None, None, 0, None) == binding.AAREN_ERR_INVALID
+    # step / init
+    assert lib.aaren_step(fake, fake, fake, fake, fake, fake, fake, 4, 40, 0, None) == binding.AAREN_ERR_UNSUPPORTED
+    assert lib.aaren_step(fake, fake, None, fake, fake, fake, fake, 4, 64, 0, None) == binding.AAREN_ERR_INVALID
+    assert lib.aaren_state_init(fake, fake, fake, -3, 64, None) == binding.AAREN_ERR_INVALID
+    # empty problems are no-ops that touch nothing
+    assert lib.aaren_scan_forward(None, None, None, None, 0, 4, 8, 64, 0, None) == binding.AAREN_OK
+    assert lib.aaren_step(None, None, None, None, None, None, None, 0, 64, 0, None) == binding.AAREN_OK
+    assert lib.aaren_state_init(None, None, None, 0, 64, None) == binding.AAREN_OK
+
+
+def test_debug_hook_is_host_state(lib):
+    assert lib.aaren_debug_set_fault(5, 1000) == 0
+    assert lib.aaren_debug_set_fault(-1, 0) == 0
+
+
+def test_no_cpu_fallback_without_library(tmp_path):
+    with pytest.raises(RuntimeError, match="no CPU fallback"):
+        binding.load(str(tmp_path / "missing.so"))
+
+
+def test_product_code_never_touches_the_oracle():
+    pkg = os.path.join(ROOT, "attention_prefix_scan_02_b300")
+    for dirpath, _, files in os.walk(pkg):
+        for fn in files:
+            if fn.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, fn)).read()
+                assert "import oracle" not in text and "from oracle" not in text, fn
+                assert "liboracle" not in text and "oracle.c" not in text, fn

@@ -1,0 +1,138 @@
+"""GPU parity: the CUDA scan (through the C ABI) against the float64 oracle on
+the named synthetic workloads, element by element.
+
+Tolerances (the oracle is fed the identical stored input values):
+  float32 inputs/outputs          row-wise relative error <= 2e-5
+  bfloat16 inputs, float32 output row-wise relative error <= 2e-3
+  bfloat16 inputs, bfloat16 output every element within 1 bf16 ulp of the
+                                  oracle rounded to bfloat16
+  final states (m, u, w)          the same bound as the outputs
+"""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from attention_prefix_scan_02_b300 import binding, inputs
+from tests.parity import (TOL_BF16, TOL_F32, bf16_ulp_violations, rowwise_rel, state_errors)
+
+pytestmark = pytest.mark.gpu
+
+THREADS = inputs.default_threads()
+
+
+def report(name, **vals):
+    print("PARITY", name, " ".join(f"{k}={v:.3e}" if isinstance(v, float) else f"{k}={v}"
+                                   for k, v in vals.items()))
+
+
+def oracle_heads(q, K, V, want_O=True):
+    """Oracle over CPU tensors q [B,H,d], K/V [B,H,N,d] (any float dtype)."""
+    B, H, N, d = K.shape
+    f = lambda t: t.to(torch.float32).reshape(-1, *t.shape[2:]).numpy()
+    return oracle.scan_heads(f(q), f(K), f(V), threads=THREADS, want_O=want_O)
+
+
+def run(qc, Kc, Vc, out_dtype, init=None):
+    q, K, V = qc.cuda(), Kc.cuda(), Vc.cuda()
+    O, (m, u, w) = binding.scan_forward(q, K, V, out_dtype=out_dtype, init=init,
+                                        return_state=True)
+    assert binding.aaren_check() == binding.AAREN_OK
+    return O.cpu(), m.cpu(), u.cpu(), w.cpu()
+
+
+def check(name, O, m, u, w, ref, tol, bf16_out=False):
+    Oref, mref, uref, wref = ref
+    B, H, N, d = O.shape
+    Oref = Oref.reshape(B, H, N, d)
+    assert torch.isfinite(O.float()).all()
+    em, ew, eu = state_errors(m, u, w, mref, uref, wref)
+    if bf16_out:
+        bad = bf16_ulp_violations(O, Oref)
+        err = rowwise_rel(O.float(), Oref)
+        report(name, out_rowwise_rel=err, bf16_ulp_violations=bad, m=em, w=ew, u=eu)
+        assert bad == 0
+    else:
+        err = rowwise_rel(O, Oref)
+        report(name, out_rowwise_rel=err, m=em, w=ew, u=eu)
+        assert err <= tol
+    assert em <= tol and ew <= tol and eu <= tol
+
+
+def test_tiny_f32():
+    wl = inputs.WORKLOADS["tiny"]
+    q, K, V = inputs.batch_inputs(wl)
+    O, m, u, w = run(q, K, V, torch.float32)
+    ref = oracle_heads(q, K, V)
+    check("tiny_f32", O, m, u, w, ref, TOL_F32)
+
+
+@pytest.mark.parametrize("out", ["f32", "bf16"])
+def test_bf16_4k(out):
+    wl = inputs.WORKLOADS["bf16_4k"]
+    q, K, V = inputs.batch_inputs(wl)
+    odt = torch.float32 if out == "f32" else torch.bfloat16
+    O, m, u, w = run(q, K, V, odt)
+    ref = oracle_heads(q, K, V)
+    check(f"bf16_4k_{out}out", O, m, u, w, ref, TOL_BF16, bf16_out=(out == "bf16"))
+
+
+def test_stress_f32():
+    wl = inputs.WORKLOADS["stress"]
+    q, K, V = inputs.batch_inputs(wl)
+    O, m, u, w = run(q, K, V, torch.float32)
+    ref = oracle_heads(q, K, V)
+    s_max = float(np.max(ref[1]))
+    report("stress_logits", max_final_m=s_max)
+    assert s_max > 150.0    # the recipe's scores are far beyond exp overflow in float32
+    check("stress_f32", O, m, u, w, ref, TOL_F32)
+
+
+@pytest.mark.parametrize("out", ["bf16", "f32"])
+def test_long_bf16_sampled(out):
+    """The 2^20-token workload at full size, in the launch configuration the
+    benchmark times: every head's final state against the oracle, and the
+    full output of a first, a middle and the last head."""
+    from concurrent.futures import ThreadPoolExecutor
+    wl = inputs.WORKLOADS["long"]
+    q, K, V = inputs.batch_inputs(wl, device="cuda")
+    odt = torch.float32 if out == "f32" else torch.bfloat16
+    O, (m, u, w) = binding.scan_forward(q, K, V, out_dtype=odt, return_state=True)
+    assert binding.aaren_check() == binding.AAREN_OK
+    del K, V
+    m, u, w = m.cpu(), u.cpu(), w.cpu()
+    sampled = (0, 7, wl.H - 1)
+    O_s = {h: O[0, h].cpu() for h in sampled}
+    del O
+
+    def one(h):
+        qh, Kh, Vh = inputs.head_inputs(wl, 0, h)
+        Oref, mr, ur, wr = oracle.scan(qh, Kh, Vh, want_O=(h in sampled))
+        res = {"state": (mr, ur, wr)}
+        if h in sampled:
+            Oh = O_s[h]
+            res["finite"] = bool(torch.isfinite(Oh.float()).all())
+            res["err"] = rowwise_rel(Oh.float(), Oref)
+            if out == "bf16":
+                res["bad"] = bf16_ulp_violations(Oh, Oref)
+        return h, res
+
+    with ThreadPoolExecutor(max_workers=max(1, min(THREADS, 8))) as ex:
+        results = dict(ex.map(one, range(wl.H)))
+    for h in sampled:
+        r = results[h]
+        assert r["finite"]
+        if out == "bf16":
+            report(f"long_{out}out_head{h}", bf16_ulp_violations=r["bad"], out_rowwise_rel=r["err"])
+            assert r["bad"] == 0
+        else:
+            report(f"long_{out}out_head{h}", out_rowwise_rel=r["err"])
+            assert r["err"] <= TOL_BF16
+    ms = np.array([results[h]["state"][0] for h in range(wl.H)])
+    us = np.array([results[h]["state"][1] for h in range(wl.H)])
+    ws = np.array([results[h]["state"][2] for h in range(wl.H)])
+    em, ew, eu = state_errors(m, u, w, ms, us, ws)
+    report(f"long_{out}out_states", m=em, w=ew, u=eu)
+    assert em <= TOL_BF16 and ew <= TOL_BF16 and eu <= TOL_BF16

@@ -1,0 +1,120 @@
+"""GPU parity of the streaming one-token update (aaren_step) on the streaming
+workload: 256 streams x 8 heads, d = 64, float32, 4096 tokens fed one step at
+a time.  The outputs and final states must match the oracle, and match
+aaren_scan_forward run on the same sequences."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from attention_prefix_scan_02_b300 import binding, inputs
+from tests.parity import TOL_BF16, TOL_F32, rowwise_rel, state_errors
+
+pytestmark = pytest.mark.gpu
+
+
+def stream_inputs(wl):
+    q, K, V = inputs.batch_inputs(wl)            # [B,H,d], [B,H,N,d]; B = streams
+    n = wl.B * wl.H
+    return q, K, V, n
+
+
+def run_steps(q, K, V, n, out_dtype, graph=False):
+    B, H, N, d = K.shape
+    qs = q.reshape(n, d).cuda()
+    Ks = K.permute(2, 0, 1, 3).reshape(N, n, d).contiguous().cuda()
+    Vs = V.permute(2, 0, 1, 3).reshape(N, n, d).contiguous().cuda()
+    Os = torch.empty((N, n, d), dtype=out_dtype, device="cuda")
+    m = torch.empty(n, device="cuda")
+    u = torch.empty(n, d, device="cuda")
+    w = torch.empty(n, device="cuda")
+    binding.aaren_state_init(m, u, w)
+    if not graph:
+        for t in range(N):
+            binding.aaren_step(qs, m, u, w, Ks[t], Vs[t], Os[t])
+    else:
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            for t in range(N):
+                binding.aaren_step(qs, m, u, w, Ks[t], Vs[t], Os[t])
+        g.replay()
+    assert binding.aaren_check() == 0
+    return Os, m, u, w
+
+
+def test_stream_workload_steps_match_oracle_and_scan():
+    wl = inputs.WORKLOADS["stream"]
+    q, K, V, n = stream_inputs(wl)
+    N, d = wl.N, wl.d
+    Os, m, u, w = run_steps(q, K, V, n, torch.float32)
+    # oracle: every stream's final state and last output
+    f = lambda t: t.reshape(n, *t.shape[2:]).numpy()
+    Oref, mref, uref, wref = oracle.scan_heads(f(q), f(K), f(V), threads=inputs.default_threads(),
+                                               want_O=False)
+    em, ew, eu = state_errors(m.cpu(), u.cpu(), w.cpu(), mref, uref, wref)
+    last_ref = uref / wref[:, None]
+    e_last = rowwise_rel(Os[-1].cpu(), last_ref)
+    print(f"PARITY stream_steps m={em:.3e} w={ew:.3e} u={eu:.3e} o_last={e_last:.3e}")
+    assert max(em, ew, eu, e_last) <= TOL_F32
+    # every step's output for a sample of streams
+    for i in (0, 1, 777, n - 1):
+        Oi, *_ = oracle.scan(f(q)[i], f(K)[i], f(V)[i])
+        assert rowwise_rel(Os[:, i].cpu(), Oi) <= TOL_F32
+    # the parallel scan on the same sequences
+    O_scan, (ms, us, ws) = binding.scan_forward(q.cuda(), K.cuda(), V.cuda(), return_state=True)
+    assert binding.aaren_check() == 0
+    es = state_errors(ms.cpu(), us.cpu(), ws.cpu(), mref, uref, wref)
+    assert max(es) <= TOL_F32
+    d_last = rowwise_rel(Os[-1].cpu(), O_scan[:, :, -1].reshape(n, d).cpu().numpy())
+    print(f"PARITY stream_step_vs_scan o_last={d_last:.3e}")
+    assert d_last <= 2 * TOL_F32
+
+
+def test_steps_in_a_cuda_graph_match_plain_launches():
+    wl = inputs.custom(16, 8, 300, 64, seed=4, kind="stream")
+    q, K, V, n = stream_inputs(wl)
+    O1, m1, u1, w1 = run_steps(q, K, V, n, torch.float32)
+    O2, m2, u2, w2 = run_steps(q, K, V, n, torch.float32, graph=True)
+    assert torch.equal(O1, O2) and torch.equal(m1, m2) and torch.equal(u1, u2)
+
+
+@pytest.mark.parametrize("d", [16, 32, 64, 128])
+@pytest.mark.parametrize("dt", ["f32", "bf16", "bf16_f32out"])
+def test_step_all_shapes(d, dt):
+    in_dtype = "f32" if dt == "f32" else "bf16"
+    out_t = torch.bfloat16 if dt == "bf16" else torch.float32
+    tol = TOL_F32 if dt == "f32" else TOL_BF16
+    wl = inputs.custom(3, 5, 70, d, dtype=in_dtype, seed=90 + d, kind="stream")
+    q, K, V, n = stream_inputs(wl)
+    Os, m, u, w = run_steps(q, K, V, n, out_t)
+    f = lambda t: t.float().reshape(n, *t.shape[2:]).numpy()
+    Oref, mref, uref, wref = oracle.scan_heads(f(q), f(K), f(V))
+    em, ew, eu = state_errors(m.cpu(), u.cpu(), w.cpu(), mref, uref, wref)
+    assert max(em, ew, eu) <= tol
+    O = Os.float().permute(1, 0, 2).cpu().numpy()
+    err = rowwise_rel(O, Oref)
+    bound = tol if dt != "bf16" else TOL_BF16 + 2.0 ** -8
+    assert err <= bound
+
+
+def test_step_continues_a_scan():
+    """Prefill with the scan, then continue the same streams with steps."""
+    wl = inputs.custom(4, 4, 600, 64, seed=44, kind="stream")
+    q, K, V, n = stream_inputs(wl)
+    cut = 450
+    d = wl.d
+    _, (m, u, w) = binding.scan_forward(q.cuda(), K[:, :, :cut].contiguous().cuda(),
+                                        V[:, :, :cut].contiguous().cuda(), return_state=True)
+    qs = q.reshape(n, d).cuda()
+    o = torch.empty(n, d, device="cuda")
+    for t in range(cut, wl.N):
+        binding.aaren_step(qs, m, u, w, K[:, :, t].reshape(n, d).contiguous().cuda(),
+                           V[:, :, t].reshape(n, d).contiguous().cuda(), o)
+    assert binding.aaren_check() == 0
+    f = lambda t: t.reshape(n, *t.shape[2:]).numpy()
+    Oref, mref, uref, wref = oracle.scan_heads(f(q), f(K), f(V))
+    em, ew, eu = state_errors(m.cpu(), u.cpu(), w.cpu(), mref, uref, wref)
+    assert max(em, ew, eu) <= TOL_F32
+    assert rowwise_rel(o.cpu(), Oref[:, -1]) <= TOL_F32
