@@ -271,6 +271,7 @@ aaren_status_t aaren_scan_forward_ex(const void *q, const void *K, const void *V
             p.states = reinterpret_cast<float *>(base + wl.states_off);
             p.status = status;
             p.N = N;
+            p.heads = BH;
             p.chunks_per_head = wl.chunks_per_head;
             p.fault_chunk = g_fault_chunk.load();
             p.wait_limit_ns = g_wait_limit_ns.load();

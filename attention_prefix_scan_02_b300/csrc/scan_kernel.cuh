@@ -64,6 +64,7 @@ struct ScanParams {
     float *states;       // workspace: per chunk [aggregate | inclusive] states
     unsigned *status;    // device status word
     int64_t N;
+    int64_t heads;           // B * H
     int64_t chunks_per_head;
     int64_t fault_chunk;     // testing: chunk that never publishes (-1 = none)
     int64_t wait_limit_ns;
@@ -182,28 +183,6 @@ __device__ __forceinline__ bool wait_bar(uint64_t *bar, unsigned parity, int64_t
     }
 }
 
-// Bounded wait (whole warp) until a chunk's flag is set; returns the flag seen
-// by lane 0, after every lane's own acquire load has seen a flag at least as
-// far along, or FLAG_NONE when the wait gave up.
-__device__ __forceinline__ unsigned wait_flag(const unsigned *flag, int64_t limit_ns, int lane)
-{
-    uint64_t t0 = 0;
-    unsigned sleep_ns = 32;
-    for (unsigned polls = 0;; ++polls) {
-        const unsigned f = ptx::ld_acquire(flag);
-        const unsigned f0 = __shfl_sync(kFull, f, 0);
-        if (__all_sync(kFull, f0 != FLAG_NONE && f >= f0)) return f0;
-        if (polls == 0) t0 = ptx::globaltimer();
-        if (polls >= kMinWaitPolls) {
-            int give_up = 0;
-            if (lane == 0) give_up = int64_t(ptx::globaltimer() - t0) > limit_ns;
-            if (__shfl_sync(kFull, give_up, 0)) return FLAG_NONE;
-        }
-        __nanosleep(sleep_ns);
-        if (sleep_ns < 1024) sleep_ns *= 2;
-    }
-}
-
 template <int D>
 __device__ __forceinline__ void read_state_smem(const float *st, float &m,
                                                 float (&u)[VLayout<D>::E], float &w, int lane)
@@ -239,34 +218,85 @@ __device__ __forceinline__ void publish_flag(unsigned *flag, unsigned value, int
     if (lane == 0) ptx::st_release(flag, value);
 }
 
-// Decoupled look-back (warp 0): fold predecessor states, nearest first,
-// until an inclusive prefix is met.  x := pred (+) x.  False on give-up or
-// poison.
+// Decoupled look-back (warp 0), 32 predecessors at a time: lane i watches
+// chunk j0 - i of the same head.  Once every lane up to the nearest inclusive
+// prefix (lane k) has a flag, lanes 0..k are folded in one pass: the scalar
+// parts (m_i, w_i) lane-parallel, the d-wide u_i by every lane over its dims.
+// x := (window) (+) x, repeated one window further back until an inclusive
+// prefix was met.  False when a wait gave up or a predecessor was poisoned.
 template <int D>
-__device__ bool lookback(const ScanParams &p, int64_t chunk, int64_t c, float &xm,
+__device__ bool lookback(const ScanParams &p, int64_t head, int64_t c, float &xm,
                          float (&xu)[VLayout<D>::E], float &xw, int lane)
 {
     using L = VLayout<D>;
+    constexpr int E = L::E;
     constexpr int SS = StateLayout<D>::SS;
-    const int64_t first = chunk - c;
-    for (int64_t pc = chunk - 1; pc >= first; --pc) {
-        const unsigned f = wait_flag(p.flags + pc, p.wait_limit_ns, lane);
-        if (f != FLAG_AGG && f != FLAG_INC) return false;
-        const float *st = p.states + (size_t(pc) * 2 + (f == FLAG_INC ? 1 : 0)) * SS;
-        const float pm = ptx::ld_relaxed(st);
-        const float pw = ptx::ld_relaxed(st + 1);
-        float pu[L::E];
-        if (L::LANES == 32 || lane < L::LANES) {
-            const float *src = st + 4 + lane * L::E;
-            if constexpr (L::E == 4) ptx::ld_relaxed4(src, pu[0], pu[1], pu[2], pu[3]);
-            else if constexpr (L::E == 2) ptx::ld_relaxed2(src, pu[0], pu[1]);
-            else pu[0] = ptx::ld_relaxed(src);
-        } else {
-#pragma unroll
-            for (int e = 0; e < L::E; ++e) pu[e] = 0.f;
+    const int64_t first = head * p.chunks_per_head;   // chunk 0 of this head
+    const bool owns = (L::LANES == 32 || lane < L::LANES);
+    for (int64_t j0 = c - 1; j0 >= 0; j0 -= 32) {
+        const int64_t j = j0 - lane;
+        const bool has = (j >= 0);                       // lanes before chunk 0 act as a stop
+        const unsigned *fp = p.flags + first + (has ? j : 0);
+        unsigned f = FLAG_INC;
+        unsigned inc = 0;
+        int k = 31;
+        uint64_t t0 = 0;
+        unsigned sleep_ns = 32;
+        for (unsigned polls = 0;; ++polls) {
+            if (has) f = ptx::ld_acquire(fp);
+            inc = __ballot_sync(kFull, f == FLAG_INC);
+            const unsigned none = __ballot_sync(kFull, f == FLAG_NONE);
+            const unsigned poison = __ballot_sync(kFull, f == FLAG_POISON);
+            k = inc ? __ffs(inc) - 1 : 31;
+            const unsigned upto = (k == 31) ? kFull : ((2u << k) - 1u);   // lanes 0..k
+            if (poison & upto) return false;
+            if (!(none & upto)) break;
+            if (polls == 0) t0 = ptx::globaltimer();
+            if (polls >= kMinWaitPolls) {
+                int give_up = 0;
+                if (lane == 0) give_up = int64_t(ptx::globaltimer() - t0) > p.wait_limit_ns;
+                if (__shfl_sync(kFull, give_up, 0)) return false;
+            }
+            __nanosleep(sleep_ns);
+            if (sleep_ns < 1024) sleep_ns *= 2;
         }
-        combine_into<L::E>(pm, pu, pw, xm, xu, xw);
-        if (f == FLAG_INC) return true;
+        // scalars of predecessor (lane) i <= k, each read by the lane that saw its flag
+        const bool in = has && lane <= k;
+        const float *st = p.states + (size_t(first + (has ? j : 0)) * 2 + (f == FLAG_INC ? 1 : 0)) * SS;
+        float mi = -INFINITY, wi = 0.f;
+        if (in) {
+            mi = ptx::ld_relaxed(st);
+            wi = ptx::ld_relaxed(st + 1);
+        }
+        const float M = fmaxf(warp_max(mi), xm);
+        const float ei = in ? exp_rel(mi, M) : 0.f;
+        const float wsum = warp_sum(ei * wi);
+        float acc[E];
+#pragma unroll
+        for (int e = 0; e < E; ++e) acc[e] = 0.f;
+        const float *st_lane0 = st;
+#pragma unroll 8
+        for (int i = 0; i < 32; ++i) {
+            if (i > k) break;
+            const float ew = __shfl_sync(kFull, ei, i);
+            const float *sti = reinterpret_cast<const float *>(
+                __shfl_sync(kFull, reinterpret_cast<uintptr_t>(st_lane0), i));
+            if (owns && ew != 0.f) {
+                float v[E];
+                const float *src = sti + 4 + lane * E;
+                if constexpr (E == 4) ptx::ld_relaxed4(src, v[0], v[1], v[2], v[3]);
+                else if constexpr (E == 2) ptx::ld_relaxed2(src, v[0], v[1]);
+                else v[0] = ptx::ld_relaxed(src);
+#pragma unroll
+                for (int e = 0; e < E; ++e) acc[e] = fmaf(ew, v[e], acc[e]);
+            }
+        }
+        const float ex = (xm == -INFINITY) ? 0.f : exp_rel(xm, M);
+#pragma unroll
+        for (int e = 0; e < E; ++e) xu[e] = fmaf(ex, xu[e], acc[e]);
+        xw = fmaf(ex, xw, wsum);
+        xm = M;
+        if (inc != 0) return true;   // lane k held an inclusive prefix (or the head start)
     }
     return true;
 }
@@ -363,9 +393,13 @@ __global__ void __launch_bounds__(WARPS * 32)
         ptx::fence_barrier_init();
     }
     __syncthreads();
-    const int64_t chunk = *s_chunk;
-    const int64_t head = chunk / p.chunks_per_head;
-    const int64_t c = chunk - head * p.chunks_per_head;
+    // tickets interleave the heads (ticket = c * heads + head), so the chunks
+    // in flight spread over all heads and their carries progress in parallel;
+    // within a head, chunk c - 1 always has an earlier ticket than chunk c
+    const int64_t ticket = *s_chunk;
+    const int64_t c = ticket / p.heads;
+    const int64_t head = ticket - c * p.heads;
+    const int64_t chunk = head * p.chunks_per_head + c;   // workspace slot
     const int64_t t0 = c * C;
     const int nvalid = static_cast<int>(p.N - t0 < C ? p.N - t0 : C);
     const int64_t row0 = head * p.N + t0;
@@ -475,7 +509,7 @@ __global__ void __launch_bounds__(WARPS * 32)
                 write_state<D>(my_state, am, au, aw, lane);
                 publish_flag(my_flag, FLAG_AGG, lane);
             }
-            ok = lookback<D>(p, chunk, c, xm, xu, xw, lane);
+            ok = lookback<D>(p, head, c, xm, xu, xw, lane);
         }
         if (ok) {
             float im = am, iw = aw, iu[E];
