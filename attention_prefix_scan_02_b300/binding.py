@@ -34,7 +34,11 @@ EXPORTS = (
     "aaren_scan_forward", "aaren_scan_forward_ex", "aaren_scan_workspace_bytes",
     "aaren_state_init", "aaren_step", "aaren_check", "aaren_status_string",
     "aaren_abi_version", "aaren_debug_set_fault", "aaren_scan_chunk_tokens",
+    "aaren_scan_forward_noalloc",
 )
+
+# size of the fixed device scratch of aaren_scan_forward_noalloc (include/aaren.h)
+AAREN_NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
 
 _lib = None
 
@@ -81,6 +85,8 @@ def load(path: str | None = None):
     lib.aaren_debug_set_fault.restype = _i32
     lib.aaren_scan_chunk_tokens.argtypes = [_i64, _i32]
     lib.aaren_scan_chunk_tokens.restype = _i64
+    lib.aaren_scan_forward_noalloc.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i32, _vp]
+    lib.aaren_scan_forward_noalloc.restype = _i32
     if path is None:
         _lib = lib
     return lib
@@ -181,6 +187,23 @@ def aaren_scan_forward_ex(q, K, V, O, m_in=None, u_in=None, w_in=None, m_out=Non
         _ptr(m_in), _ptr(u_in), _ptr(w_in), _ptr(m_out), _ptr(u_out), _ptr(w_out),
         _ptr(workspace), ws_bytes, _stream_handle(stream))
     _raise(rc, "aaren_scan_forward_ex")
+    return O
+
+
+def aaren_scan_forward_noalloc(q, K, V, O, stream=None):
+    """aaren_scan_forward without any device allocation: the carry workspace is
+    the library's fixed device array (see include/aaren.h for the limit and
+    the rule that calls overlapping on the GPU race)."""
+    lib = load()
+    if K.dim() != 4 or tuple(V.shape) != tuple(K.shape) or tuple(O.shape) != tuple(K.shape):
+        raise ValueError("K, V and O must have the same shape [B, H, N, d]")
+    B, H, N, d = K.shape
+    if tuple(q.shape) != (B, H, d) or q.dtype != K.dtype or V.dtype != K.dtype:
+        raise ValueError("q must be [B, H, d] and share the dtype of K and V")
+    _check_cuda(q, K, V, O)
+    rc = lib.aaren_scan_forward_noalloc(_ptr(q), _ptr(K), _ptr(V), _ptr(O), B, H, N, d,
+                                        dtype_code(K.dtype, O.dtype), _stream_handle(stream))
+    _raise(rc, "aaren_scan_forward_noalloc")
     return O
 
 

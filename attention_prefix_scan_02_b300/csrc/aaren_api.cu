@@ -370,3 +370,52 @@ int64_t aaren_scan_chunk_tokens(int64_t d, int32_t dtype)
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free scan: the same scan with its cross-block carry workspace in
+// a fixed device array of this library instead of memory the caller or the
+// stream-ordered allocator provides.
+// ---------------------------------------------------------------------------
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[AAREN_NOALLOC_SCRATCH_BYTES];
+
+namespace aaren {
+namespace {
+
+constexpr int kMaxNoallocDevices = 64;
+std::atomic<void *> g_noalloc_scratch_ptr[kMaxNoallocDevices];
+
+// Device address of g_noalloc_scratch on the current device, looked up once
+// per device (the array's name in host code is only a host-side handle).
+aaren_status_t noalloc_scratch(void **out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxNoallocDevices)
+        return AAREN_ERR_CUDA;
+    void *ptr = g_noalloc_scratch_ptr[dev].load();
+    if (ptr == nullptr) {
+        if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr)
+            return AAREN_ERR_CUDA;
+        g_noalloc_scratch_ptr[dev].store(ptr);
+    }
+    *out = ptr;
+    return AAREN_OK;
+}
+
+}  // namespace
+}  // namespace aaren
+
+extern "C" aaren_status_t aaren_scan_forward_noalloc(const void *q, const void *K, const void *V,
+                                                     void *O, int64_t B, int64_t H, int64_t N,
+                                                     int64_t d, int32_t dtype, void *stream)
+{
+    void *scratch = nullptr;
+    const aaren_status_t rc = noalloc_scratch(&scratch);
+    if (rc != AAREN_OK) return rc;
+    // The regular path with a caller workspace allocates nothing: it zeroes
+    // the ticket and flags of the workspace (cudaMemsetAsync) and launches.
+    // A problem whose workspace exceeds the array is rejected there with
+    // AAREN_ERR_WORKSPACE before anything is launched.
+    return aaren_scan_forward_ex(q, K, V, O, B, H, N, d, dtype, nullptr, nullptr, nullptr, nullptr,
+                                 nullptr, nullptr, scratch, AAREN_NOALLOC_SCRATCH_BYTES, stream);
+}

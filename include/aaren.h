@@ -178,6 +178,42 @@ aaren_status_t aaren_debug_set_fault(int64_t never_publish_chunk,
  * (0 if unsupported); the chunk index of aaren_debug_set_fault counts these. */
 int64_t aaren_scan_chunk_tokens(int64_t d, int32_t dtype);
 
+/*
+ * aaren_scan_forward_noalloc -- aaren_scan_forward for callers that must not
+ * allocate device memory.  The pages have no counterpart: this is a
+ * deployment variant of the same scan.
+ *
+ * Who needs it: code whose GPU memory is owned by another allocator (a host
+ * framework or plugin host that reserves the device and forbids outside
+ * cudaMalloc), and latency-critical loops that cannot risk an allocator call,
+ * which may block or fail when memory is full or fragmented.  Such callers
+ * pass inputs and outputs exactly as for aaren_scan_forward (same arguments,
+ * layouts and errors); the scan's cross-block carry workspace then lives in
+ * a fixed array of AAREN_NOALLOC_SCRATCH_BYTES inside this library, which
+ * every GPU that loads the library keeps until the process exits.
+ *
+ * Limits and behaviour:
+ *  - A problem whose workspace, aaren_scan_workspace_bytes(B,H,N,d), exceeds
+ *    AAREN_NOALLOC_SCRATCH_BYTES is rejected with AAREN_ERR_WORKSPACE before
+ *    anything runs (with d = 128 that is one to two million tokens over all
+ *    heads, depending on the dtype's chunk size; smaller d allow more).
+ *  - No cudaMalloc, cudaFree or other allocating call is made.  The part of
+ *    the array that must start at zero is cleared on `stream` by every call.
+ *  - The first call on a device looks up the array's device address (once per
+ *    device); make that first call before any stream capture.
+ *  - All calls on a device share the one array, which keeps the last call's
+ *    contents: calls whose executions overlap on the GPU (different streams
+ *    without ordering between them) race and corrupt each other's results.
+ *    Order them on one stream, or use aaren_scan_forward_ex with separate
+ *    workspaces.
+ */
+#define AAREN_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+
+aaren_status_t aaren_scan_forward_noalloc(const void *q, const void *K,
+                                          const void *V, void *O, int64_t B,
+                                          int64_t H, int64_t N, int64_t d,
+                                          int32_t dtype, void *stream);
+
 #ifdef __cplusplus
 }
 #endif
