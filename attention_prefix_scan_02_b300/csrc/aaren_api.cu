@@ -12,6 +12,7 @@
 #include "aaren.h"
 #include "common.cuh"
 #include "scan_kernel.cuh"
+#include "scan_pipe_kernel.cuh"
 #include "step_kernel.cuh"
 
 namespace aaren {
@@ -116,14 +117,61 @@ aaren_status_t launch_scan(const ScanParams &p, int64_t total_chunks, cudaStream
     return cudaGetLastError() == cudaSuccess ? AAREN_OK : AAREN_ERR_CUDA;
 }
 
+// Groups per block of the persistent bfloat16 kernel, per d: each group
+// holds one 128-token stage of K and V (64 KB at d = 128) and five warps.
+#ifndef AAREN_PIPE_GROUPS_D128
+#define AAREN_PIPE_GROUPS_D128 3
+#endif
+#ifndef AAREN_PIPE_GROUPS_D64
+#define AAREN_PIPE_GROUPS_D64 4
+#endif
+template <int D>
+struct PipeChoice {
+    static constexpr int GROUPS = (D == 128) ? AAREN_PIPE_GROUPS_D128 : (D == 64 ? AAREN_PIPE_GROUPS_D64 : 4);
+};
+
+int sm_count()
+{
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return n;
+}
+
+template <int D, typename Tout>
+aaren_status_t launch_pipe(const ScanParams &p, int64_t total_chunks, cudaStream_t st)
+{
+    using PC = PipeChoice<D>;
+    using Tile = PipeTile<D, PC::GROUPS>;
+    static std::atomic<unsigned long long> configured{0};
+    auto kern = k_scan_pipe<D, Tout, PC::GROUPS>;
+    if (allow_smem(kern, Tile::smem_bytes, configured) != cudaSuccess) return AAREN_ERR_CUDA;
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, Tile::THREADS,
+                                                      Tile::smem_bytes) != cudaSuccess ||
+        per_sm < 1)
+        return AAREN_ERR_CUDA;
+    const int sms = sm_count();
+    if (sms <= 0) return AAREN_ERR_CUDA;
+    int64_t grid = int64_t(sms) * per_sm;
+    if (grid > total_chunks) grid = total_chunks;
+    kern<<<unsigned(grid), Tile::THREADS, Tile::smem_bytes, st>>>(p, total_chunks);
+    return cudaGetLastError() == cudaSuccess ? AAREN_OK : AAREN_ERR_CUDA;
+}
+
 template <int D>
 aaren_status_t dispatch_scan_dtype(const ScanParams &p, int64_t total, int32_t dtype,
                                    cudaStream_t st)
 {
     switch (dtype) {
     case AAREN_F32: return launch_scan<D, float, float>(p, total, st);
+#ifdef AAREN_BF16_BLOCK_KERNEL
     case AAREN_BF16: return launch_scan<D, __nv_bfloat16, __nv_bfloat16>(p, total, st);
     case AAREN_BF16_F32OUT: return launch_scan<D, __nv_bfloat16, float>(p, total, st);
+#else
+    case AAREN_BF16: return launch_pipe<D, __nv_bfloat16>(p, total, st);
+    case AAREN_BF16_F32OUT: return launch_pipe<D, float>(p, total, st);
+#endif
     default: return AAREN_ERR_UNSUPPORTED;
     }
 }

@@ -1,6 +1,6 @@
 // ptx.cuh -- thin inline-PTX wrappers used by the kernels (sm_103a):
-// global timer, acquire/release flag accesses at GPU scope, mbarrier and the
-// 1-D bulk copy (TMA) from global to shared memory.
+// global timer, acquire/release flag accesses at GPU scope, mbarriers, named
+// barriers and the 1-D bulk copy (TMA) from global to shared memory.
 #pragma once
 
 #include <cstdint>
@@ -25,6 +25,15 @@ __device__ __forceinline__ unsigned ld_acquire(const unsigned *p)
 __device__ __forceinline__ void st_release(unsigned *p, unsigned v)
 {
     asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Compare-and-swap with release semantics at GPU scope; returns the old value.
+__device__ __forceinline__ unsigned cas_release(unsigned *p, unsigned cmp, unsigned v)
+{
+    unsigned old;
+    asm volatile("atom.release.gpu.global.cas.b32 %0, [%1], %2, %3;"
+                 : "=r"(old) : "l"(p), "r"(cmp), "r"(v) : "memory");
+    return old;
 }
 
 __device__ __forceinline__ float ld_relaxed(const float *p)
@@ -78,6 +87,33 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, unsigned parity)
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Plain arrival (no transaction bytes) on an mbarrier.
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+// Barrier `id` (1..15) over `threads` threads (a multiple of 32) of the
+// block; the non-aligned form, so lanes may arrive from divergent code.
+__device__ __forceinline__ void named_bar_sync(unsigned id, unsigned threads)
+{
+    asm volatile("barrier.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// Non-blocking test of an mbarrier phase (never suspends the thread).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, unsigned parity)
+{
+    unsigned ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
         : "r"(smem_addr(bar)), "r"(parity)

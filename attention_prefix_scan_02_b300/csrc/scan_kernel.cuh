@@ -210,12 +210,32 @@ __device__ __forceinline__ void write_state(float *st, float m, const float (&u)
     if (L::LANES == 32 || lane < L::LANES) store_vals<L::E>(st + 4 + lane * L::E, u);
 }
 
-// Make this warp's workspace writes visible at GPU scope, then set the flag.
+// Set a chunk's flag after this warp's workspace writes: the warp barrier
+// orders every lane's writes before lane 0's release store, which makes them
+// visible at GPU scope to any reader that acquires the flag.
 __device__ __forceinline__ void publish_flag(unsigned *flag, unsigned value, int lane)
 {
-    __threadfence();
     __syncwarp();
     if (lane == 0) ptx::st_release(flag, value);
+}
+
+// The same, but only while the flag is still FLAG_NONE (an aggregate must
+// never replace an inclusive prefix or a poison mark published meanwhile).
+__device__ __forceinline__ void publish_agg_if_none(unsigned *flag, int lane)
+{
+    __syncwarp();
+    if (lane == 0) ptx::cas_release(flag, FLAG_NONE, FLAG_AGG);
+}
+
+// Bounded wait on an mbarrier phase by spinning on the non-blocking test.
+__device__ __forceinline__ bool wait_bar_spin(uint64_t *bar, unsigned parity, int64_t limit_ns)
+{
+    if (ptx::mbar_test_wait(bar, parity)) return true;
+    const uint64_t t0 = ptx::globaltimer();
+    for (unsigned polls = 1;; ++polls) {
+        if (ptx::mbar_test_wait(bar, parity)) return true;
+        if (polls >= kMinWaitPolls && int64_t(ptx::globaltimer() - t0) > limit_ns) return false;
+    }
 }
 
 // Decoupled look-back (warp 0), 32 predecessors at a time: lane i watches
@@ -224,9 +244,16 @@ __device__ __forceinline__ void publish_flag(unsigned *flag, unsigned value, int
 // parts (m_i, w_i) lane-parallel, the d-wide u_i by every lane over its dims.
 // x := (window) (+) x, repeated one window further back until an inclusive
 // prefix was met.  False when a wait gave up or a predecessor was poisoned.
-template <int D>
+struct NoHook {
+    __device__ void operator()() const {}
+};
+
+// `hook` is called (by the whole warp) each time a poll finds a predecessor
+// without a published state, before backing off: the caller can do useful
+// work there (e.g. publish its own aggregate once it is ready).
+template <int D, int BATCH = 8, typename Hook = NoHook>
 __device__ bool lookback(const ScanParams &p, int64_t head, int64_t c, float &xm,
-                         float (&xu)[VLayout<D>::E], float &xw, int lane)
+                         float (&xu)[VLayout<D>::E], float &xw, int lane, Hook &&hook = Hook())
 {
     using L = VLayout<D>;
     constexpr int E = L::E;
@@ -257,8 +284,9 @@ __device__ bool lookback(const ScanParams &p, int64_t head, int64_t c, float &xm
                 if (lane == 0) give_up = int64_t(ptx::globaltimer() - t0) > p.wait_limit_ns;
                 if (__shfl_sync(kFull, give_up, 0)) return false;
             }
+            hook();
             __nanosleep(sleep_ns);
-            if (sleep_ns < 1024) sleep_ns *= 2;
+            if (sleep_ns < 256) sleep_ns *= 2;
         }
         // scalars of predecessor (lane) i <= k, each read by the lane that saw its flag
         const bool in = has && lane <= k;
@@ -268,29 +296,43 @@ __device__ bool lookback(const ScanParams &p, int64_t head, int64_t c, float &xm
             mi = ptx::ld_relaxed(st);
             wi = ptx::ld_relaxed(st + 1);
         }
-        const float M = fmaxf(warp_max(mi), xm);
-        const float ei = in ? exp_rel(mi, M) : 0.f;
-        const float wsum = warp_sum(ei * wi);
+        // u of predecessors 0..k, BATCH at a time: a batch's loads are all
+        // issued before any is used (one memory round trip per batch, not per
+        // predecessor), and the first batch does not wait for the scalars
         float acc[E];
 #pragma unroll
         for (int e = 0; e < E; ++e) acc[e] = 0.f;
-        const float *st_lane0 = st;
-#pragma unroll 8
-        for (int i = 0; i < 32; ++i) {
-            if (i > k) break;
-            const float ew = __shfl_sync(kFull, ei, i);
-            const float *sti = reinterpret_cast<const float *>(
-                __shfl_sync(kFull, reinterpret_cast<uintptr_t>(st_lane0), i));
-            if (owns && ew != 0.f) {
-                float v[E];
-                const float *src = sti + 4 + lane * E;
-                if constexpr (E == 4) ptx::ld_relaxed4(src, v[0], v[1], v[2], v[3]);
-                else if constexpr (E == 2) ptx::ld_relaxed2(src, v[0], v[1]);
-                else v[0] = ptx::ld_relaxed(src);
+        float ei = 0.f;
+        float M = xm;
+        for (int i0 = 0; i0 <= k; i0 += BATCH) {
+            float v[BATCH][E];
 #pragma unroll
-                for (int e = 0; e < E; ++e) acc[e] = fmaf(ew, v[e], acc[e]);
+            for (int b = 0; b < BATCH; ++b) {
+                const int i = i0 + b;
+                const unsigned fi = __shfl_sync(kFull, f, i & 31);
+                const int64_t ji = j0 - i;
+#pragma unroll
+                for (int e = 0; e < E; ++e) v[b][e] = 0.f;
+                if (owns && i <= k && ji >= 0) {
+                    const float *src = p.states + (size_t(first + ji) * 2 + (fi == FLAG_INC ? 1 : 0)) * SS +
+                                       4 + lane * E;
+                    if constexpr (E == 4) ptx::ld_relaxed4(src, v[b][0], v[b][1], v[b][2], v[b][3]);
+                    else if constexpr (E == 2) ptx::ld_relaxed2(src, v[b][0], v[b][1]);
+                    else v[b][0] = ptx::ld_relaxed(src);
+                }
+            }
+            if (i0 == 0) {
+                M = fmaxf(warp_max(mi), xm);
+                ei = in ? exp_rel(mi, M) : 0.f;
+            }
+#pragma unroll
+            for (int b = 0; b < BATCH; ++b) {
+                const float ew = __shfl_sync(kFull, ei, (i0 + b) & 31);
+#pragma unroll
+                for (int e = 0; e < E; ++e) acc[e] = fmaf(ew, v[b][e], acc[e]);
             }
         }
+        const float wsum = warp_sum(ei * wi);
         const float ex = (xm == -INFINITY) ? 0.f : exp_rel(xm, M);
 #pragma unroll
         for (int e = 0; e < E; ++e) xu[e] = fmaf(ex, xu[e], acc[e]);

@@ -1,0 +1,558 @@
+// scan_pipe_kernel.cuh -- persistent, warp-specialised form of the fused
+// score + chunked prefix scan for bfloat16 K and V (the path of the long,
+// HBM-bound workloads): the many-to-many softmax-attention output in one pass
+// over K and V.
+//
+// The method is the one of scan_kernel.cuh ("Attention as an RNN" review,
+// "Proposed method": every prefix output o_t is the inclusive prefix of the
+// associative (m, u, w) operator; "Self-attention Does Not Need O(n^2)
+// Memory" review, sections 2 and 3: running sums kept stable by the running
+// maximum).  What differs is how the work is laid out on an SM.
+//
+// One block per SM stays alive for the whole launch.  It holds GROUPS
+// independent groups; each group owns one shared-memory stage (K and V of a
+// 128-token chunk) and five warps:
+//   * four compute warps; warp w owns tokens [32w, 32w + 32) of the chunk
+//     and lane l owns dims [E l, E l + E) of every row:
+//       - scores: each lane forms its E-term share of q . k_t per row, then a
+//         transposed butterfly of shuffles leaves s_t on lane t;
+//       - V of the warp's rows is copied into registers (still bfloat16) and
+//         the stage is handed back at once ("empty" mbarrier);
+//       - warp aggregate (m, u, w) into shared memory ("agg" mbarrier);
+//       - after the carry arrives ("carry" mbarrier): rescan from registers
+//         and write O;
+//   * one carry warp that never holds V:
+//       - takes the group's chunk tickets (interleaved over heads: ticket =
+//         c * heads + head) and issues the 1-D bulk copies (TMA) of K and V;
+//       - runs the decoupled look-back over predecessor chunks while the
+//         compute warps are still scoring, publishing this chunk's aggregate
+//         as soon as the compute warps have produced it;
+//       - publishes the inclusive prefix, hands each compute warp its carry,
+//         and only then takes the group's next ticket.
+// Taking a ticket only when the group is about to need it keeps chunks
+// flowing close to ticket order, so predecessors have usually published by
+// the time a chunk looks back; the load of the next chunk overlaps the
+// rescan of the current one.  Keeping V out of the carry warp keeps the
+// register peak to the larger of the two roles.
+//
+// Forward progress: a ticket is taken only when its group's stage is free,
+// and its copy is issued at once; every group handles its chunks in ticket
+// order.  The smallest unfinished ticket is then always the one its group is
+// working on, and it waits only on smaller (finished) tickets.  Every wait is
+// bounded (%globaltimer); a wait that gives up sets a bit of the device
+// status word and the group stops.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "common.cuh"
+#include "ptx.cuh"
+#include "scan_kernel.cuh"
+
+namespace aaren {
+
+constexpr int kPipeComputeWarps = 4;
+constexpr int kPipeGroupWarps = kPipeComputeWarps + 1;
+// predecessor states folded per memory round trip in the look-back
+#ifndef AAREN_PIPE_FOLD_BATCH
+#define AAREN_PIPE_FOLD_BATCH 12
+#endif
+constexpr int kPipeFoldBatch = AAREN_PIPE_FOLD_BATCH;
+// rows per unrolled block of the rescan loop (32: fully unrolled)
+#ifndef AAREN_PIPE_RESCAN_BLOCK
+#define AAREN_PIPE_RESCAN_BLOCK 8
+#endif
+constexpr int kRescanBlock = AAREN_PIPE_RESCAN_BLOCK;
+static_assert(32 % kRescanBlock == 0, "rescan blocks must tile the warp's 32 rows");
+
+template <int D, int GROUPS_>
+struct PipeTile {
+    using Tin = __nv_bfloat16;
+    static constexpr int GROUPS = GROUPS_;
+    static constexpr int C = 32 * kPipeComputeWarps;   // tokens per chunk
+    static constexpr int THREADS = 32 * kPipeGroupWarps * GROUPS;
+    static constexpr int SS = StateLayout<D>::SS;
+    static constexpr size_t half_bytes = size_t(C) * D * sizeof(Tin);   // K (or V) of a chunk
+    static constexpr size_t q_bytes = size_t(D) * sizeof(Tin);
+    // per group: stage (K | V | q), warp aggregates (two sets), warp carries, rescan
+    // coefficients, ticket and failure word, four mbarriers
+    static constexpr size_t g_stage = 0;
+    static constexpr size_t g_q = g_stage + 2 * half_bytes;
+    static constexpr size_t g_wst = g_q + (q_bytes + 15) / 16 * 16;
+    // warp aggregates, double-buffered by chunk parity: compute warp 0 may
+    // still read a chunk's aggregates (to publish them) while the other warps
+    // write the next chunk's
+    static constexpr size_t g_cst = g_wst + 2 * size_t(kPipeComputeWarps) * SS * sizeof(float);
+    static constexpr size_t g_coef = g_cst + size_t(kPipeComputeWarps) * SS * sizeof(float);
+    static constexpr size_t g_meta = g_coef + size_t(kPipeComputeWarps) * 32 * sizeof(float4);
+    static constexpr size_t g_bars = g_meta + 16;
+    static constexpr size_t group_bytes = g_bars + 4 * sizeof(uint64_t);
+    static constexpr size_t smem_bytes = size_t(GROUPS) * group_bytes;
+    static_assert(half_bytes % 16 == 0 && g_wst % 16 == 0 && g_cst % 16 == 0 && g_coef % 16 == 0 &&
+                      g_meta % 16 == 0 && group_bytes % 16 == 0,
+                  "shared-memory regions must stay aligned");
+    static_assert(smem_bytes <= 227 * 1024, "stages do not fit in shared memory");
+};
+
+constexpr long long kTicketStop = -1;   // no chunk left for this group
+
+// E bfloat16 values of one row held in registers (lane-owned dims).
+template <int E>
+struct RawRow {
+    unsigned w[E == 4 ? 2 : 1];
+};
+
+template <int E>
+__device__ __forceinline__ void lds_row(const __nv_bfloat16 *p, RawRow<E> &r)
+{
+    if constexpr (E == 4) {
+        const uint2 v = *reinterpret_cast<const uint2 *>(p);
+        r.w[0] = v.x;
+        r.w[1] = v.y;
+    } else if constexpr (E == 2) {
+        r.w[0] = *reinterpret_cast<const unsigned *>(p);
+    } else {
+        r.w[0] = *reinterpret_cast<const unsigned short *>(p);
+    }
+}
+
+template <int E>
+__device__ __forceinline__ void unpack_row(const RawRow<E> &r, float (&f)[E])
+{
+    if constexpr (E == 4) {
+        bf16x2_to_f32(r.w[0], f[0], f[1]);
+        bf16x2_to_f32(r.w[1], f[2], f[3]);
+    } else if constexpr (E == 2) {
+        bf16x2_to_f32(r.w[0], f[0], f[1]);
+    } else {
+        f[0] = __uint_as_float(r.w[0] << 16);
+    }
+}
+
+// unpack_row with the zero bits taken from a register z (always 0) that the
+// caller loads just before the row is used.  The dependency keeps the
+// compiler from converting all 32 register-held rows at once, long before
+// they are needed (which would triple the registers V occupies).
+template <int E>
+__device__ __forceinline__ void unpack_row_late(const RawRow<E> &r, unsigned z, float (&f)[E])
+{
+    unsigned a[E];
+#pragma unroll
+    for (int k = 0; k < (E + 1) / 2; ++k) {
+        // prmt: bytes 0-3 from the row word, bytes 4-7 from z
+        asm("prmt.b32 %0, %1, %2, 0x1044;" : "=r"(a[2 * k]) : "r"(r.w[k]), "r"(z));
+        if (2 * k + 1 < E) asm("prmt.b32 %0, %1, %2, 0x3244;" : "=r"(a[2 * k + 1]) : "r"(r.w[k]), "r"(z));
+    }
+#pragma unroll
+    for (int e = 0; e < E; ++e) f[e] = __uint_as_float(a[e]);
+}
+
+// x[i] holds this lane's share of row i's dot product (i < 8).  Returns, on
+// every lane, the full sum over the 32 lanes for row (lane & 7): a butterfly
+// that halves the rows each lane keeps at every exchange (4 + 2 + 1
+// shuffles), then two exchanges that add up the four groups of eight lanes.
+__device__ __forceinline__ float transpose_sum8(float (&x)[8], int lane)
+{
+#pragma unroll
+    for (int h = 4; h >= 1; h >>= 1) {
+        const bool upper = (lane & h) != 0;
+#pragma unroll
+        for (int i = 0; i < h; ++i) {
+            const float send = upper ? x[i] : x[i + h];
+            const float keep = upper ? x[i + h] : x[i];
+            x[i] = keep + __shfl_xor_sync(kFull, send, h);
+        }
+    }
+    float y = x[0];
+    y += __shfl_xor_sync(kFull, y, 8);
+    y += __shfl_xor_sync(kFull, y, 16);
+    return y;
+}
+
+// Non-blocking test of an mbarrier phase by a whole warp: true only when
+// every lane has observed the phase complete (each lane then has acquired
+// the data released with it).
+__device__ __forceinline__ bool warp_test_bar(uint64_t *bar, unsigned parity)
+{
+    return __all_sync(kFull, ptx::mbar_try_wait(bar, parity));
+}
+
+// Combine the four compute warps' aggregates (in shared memory) into the
+// chunk's aggregate, in warp order.
+template <int D>
+__device__ __forceinline__ void chunk_aggregate(const float *wst, float &am,
+                                                float (&au)[VLayout<D>::E], float &aw, int lane)
+{
+    constexpr int E = VLayout<D>::E;
+    constexpr int SS = StateLayout<D>::SS;
+    read_state_smem<D>(wst, am, au, aw, lane);
+#pragma unroll
+    for (int k = 1; k < kPipeComputeWarps; ++k) {
+        float bm, bw, bu[E];
+        read_state_smem<D>(wst + k * SS, bm, bu, bw, lane);
+        combine_into<E>(am, au, aw, bm, bu, bw);
+        am = bm;
+        aw = bw;
+#pragma unroll
+        for (int e = 0; e < E; ++e) au[e] = bu[e];
+    }
+}
+
+#ifndef AAREN_PIPE_SPIN_WAIT
+#define AAREN_PIPE_SPIN_WAIT 0
+#endif
+// How compute warps wait for their stage and their carry.
+__device__ __forceinline__ bool compute_wait(uint64_t *bar, unsigned parity, int64_t limit_ns)
+{
+    return AAREN_PIPE_SPIN_WAIT ? wait_bar_spin(bar, parity, limit_ns) : wait_bar(bar, parity, limit_ns);
+}
+
+template <int D, typename Tout, int GROUPS>
+__global__ void __launch_bounds__(PipeTile<D, GROUPS>::THREADS, 1)
+    k_scan_pipe(const ScanParams p, const int64_t total_chunks)
+{
+    using Tin = __nv_bfloat16;
+    using L = VLayout<D>;
+    using T = PipeTile<D, GROUPS>;
+    constexpr int E = L::E;
+    constexpr int C = T::C;
+    constexpr int SS = T::SS;
+
+    extern __shared__ __align__(128) unsigned char smem[];
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int g = warp / kPipeGroupWarps;        // group
+    const int role = warp % kPipeGroupWarps;     // 0..3 compute warp, 4 carry warp
+    unsigned char *gs = smem + size_t(g) * T::group_bytes;
+    unsigned char *stage = gs + T::g_stage;
+    float *wst = reinterpret_cast<float *>(gs + T::g_wst);
+    float *cst = reinterpret_cast<float *>(gs + T::g_cst);
+    volatile long long *meta = reinterpret_cast<volatile long long *>(gs + T::g_meta);
+    volatile int *fail = reinterpret_cast<volatile int *>(gs + T::g_meta + 8);
+    uint64_t *full = reinterpret_cast<uint64_t *>(gs + T::g_bars);   // stage loaded (1 + bytes)
+    uint64_t *empty = full + 1;                                       // stage read (4 warps)
+    uint64_t *aggb = full + 2;                                        // warp aggregates written (4)
+    uint64_t *carryb = full + 3;                                      // carries written (1)
+    const bool owns = (L::LANES == 32 || lane < L::LANES);
+
+    if (role == kPipeComputeWarps && lane == 0) {
+        ptx::mbar_init(full, 1);
+        ptx::mbar_init(empty, kPipeComputeWarps);
+        ptx::mbar_init(aggb, kPipeComputeWarps);
+        ptx::mbar_init(carryb, 1);
+        ptx::fence_barrier_init();
+    }
+    __syncthreads();
+    // waits on the group's own barriers may legitimately last as long as a
+    // look-back wait, so they get a wider limit
+    const int64_t group_limit = p.wait_limit_ns * 16;
+
+    if (role == kPipeComputeWarps) {
+        // ------------------------------------------------------------ carry warp
+        const uint64_t pol = ptx::policy_evict_first();
+        bool exhausted = false;      // a stop ticket was posted
+        bool pending = false;        // a copy was issued whose phase was not yet consumed
+        // Take the group's next ticket into the (free) stage and start its copy.
+        // Returns false when the stage did not come free in time.
+        auto issue = [&](int64_t it) -> bool {
+            long long t = kTicketStop;
+            int ok = 1;
+            if (lane == 0) {
+                ok = wait_bar(empty, static_cast<unsigned>(it & 1) ^ 1u, group_limit) ? 1 : 0;
+                if (ok) {
+                    t = static_cast<long long>(atomicAdd(p.ticket, 1u));
+                    if (t >= total_chunks) t = kTicketStop;
+                    *meta = t;
+                    if (t < 0) {
+                        ptx::mbar_arrive(full);
+                    } else {
+                        const int64_t c = t / p.heads;
+                        const int64_t head = t - c * p.heads;
+                        const int64_t t0 = c * C;
+                        const int nvalid = static_cast<int>(p.N - t0 < C ? p.N - t0 : C);
+                        const unsigned bytes = static_cast<unsigned>(nvalid) * D * sizeof(Tin);
+                        const int64_t row0 = head * p.N + t0;
+                        ptx::mbar_arrive_expect_tx(full, 2 * bytes + unsigned(T::q_bytes));
+                        ptx::bulk_g2s(stage, static_cast<const Tin *>(p.K) + row0 * D, bytes, full, pol);
+                        ptx::bulk_g2s(stage + T::half_bytes, static_cast<const Tin *>(p.V) + row0 * D,
+                                      bytes, full, pol);
+                        ptx::bulk_g2s(gs + T::g_q, static_cast<const Tin *>(p.q) + head * D,
+                                      unsigned(T::q_bytes), full, pol);
+                    }
+                }
+            }
+            ok = __shfl_sync(kFull, ok, 0);
+            t = __shfl_sync(kFull, t, 0);
+            if (ok) {
+                exhausted = (t < 0);
+                pending = (t >= 0);
+            }
+            return ok != 0;
+        };
+
+        bool ok = issue(0);
+        int64_t it = 0;
+        for (; ok && !exhausted; ++it) {
+            const long long t = __shfl_sync(kFull, lane == 0 ? *meta : 0ll, 0);
+            const unsigned par = static_cast<unsigned>(it & 1);
+            const int64_t c = t / p.heads;
+            const int64_t head = t - c * p.heads;
+            const int64_t chunk = head * p.chunks_per_head + c;   // workspace slot
+            const bool publish = (chunk != p.fault_chunk);
+            unsigned *my_flag = p.flags + chunk;
+            float *my_state = p.states + size_t(chunk) * 2 * SS;
+
+            float xm = -INFINITY, xw = 0.f, xu[E];
+#pragma unroll
+            for (int e = 0; e < E; ++e) xu[e] = 0.f;
+            bool lb_ok = true;
+            if (c == 0) {
+                if (p.m_in != nullptr) {
+                    xm = p.m_in[head];
+                    xw = p.w_in[head];
+                    if (owns) load_vals<E>(p.u_in + head * D + lane * E, xu);
+                }
+            } else {
+                lb_ok = lookback<D, kPipeFoldBatch>(p, head, c, xm, xu, xw, lane);
+            }
+            // chunk aggregate from the four warp aggregates
+            if (!wait_bar(aggb, par, group_limit)) {
+                if (lane == 0) atomicOr(p.status, STATUS_LOAD_TIMEOUT);
+                break;   // the compute warps stopped
+            }
+            pending = false;   // the compute warps have consumed the copy
+            float am, aw, au[E];
+            const float *wst_it = wst + size_t(par) * kPipeComputeWarps * SS;
+            chunk_aggregate<D>(wst_it, am, au, aw, lane);
+            if (lb_ok) {
+                float im = am, iw = aw, iu[E];
+#pragma unroll
+                for (int e = 0; e < E; ++e) iu[e] = au[e];
+                combine_into<E>(xm, xu, xw, im, iu, iw);   // inclusive = exclusive (+) aggregate
+                // carry into compute warp k = exclusive (+) aggregates of warps
+                // 0..k-1, handed over before the inclusive prefix is published
+                // (only successors need that)
+#pragma unroll
+                for (int k = 0; k < kPipeComputeWarps; ++k) {
+                    write_state<D>(cst + k * SS, xm, xu, xw, lane);
+                    if (k + 1 < kPipeComputeWarps) {
+                        float bm, bw, bu[E];
+                        read_state_smem<D>(wst_it + k * SS, bm, bu, bw, lane);
+                        combine_into<E>(xm, xu, xw, bm, bu, bw);
+                        xm = bm;
+                        xw = bw;
+#pragma unroll
+                        for (int e = 0; e < E; ++e) xu[e] = bu[e];
+                    }
+                }
+                if (lane == 0) *fail = 0;
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(carryb);
+                if (publish) {
+                    write_state<D>(my_state + SS, im, iu, iw, lane);
+                    publish_flag(my_flag, FLAG_INC, lane);
+                }
+                if (c == p.chunks_per_head - 1 && p.m_out != nullptr) {
+                    if (lane == 0) {
+                        p.m_out[head] = im;
+                        p.w_out[head] = iw;
+                    }
+                    if (owns) store_vals<E>(p.u_out + head * D + lane * E, iu);
+                }
+            } else {
+                if (lane == 0) {
+                    atomicOr(p.status, STATUS_LOOKBACK_TIMEOUT);
+                    *fail = 1;
+                }
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(carryb);
+                if (publish) publish_flag(my_flag, FLAG_POISON, lane);
+            }
+            ok = issue(it + 1);
+            if (!ok && lane == 0) atomicOr(p.status, STATUS_LOAD_TIMEOUT);
+        }
+        // A copy this warp issued can still be in flight only if the compute
+        // warps stopped early: wait for it before the block's memory goes.
+        if (pending && lane == 0) wait_bar(full, static_cast<unsigned>(it & 1), group_limit);
+        return;
+    }
+
+    // ------------------------------------------------------------ compute warps
+    const int wg = role;
+    float4 *cf = reinterpret_cast<float4 *>(gs + T::g_coef) + wg * 32;
+    for (int64_t it = 0;; ++it) {
+        const unsigned par = static_cast<unsigned>(it & 1);
+        if (!compute_wait(full, par, group_limit)) {
+            if (lane == 0) atomicOr(p.status, STATUS_LOAD_TIMEOUT);
+            break;
+        }
+        const long long t = *meta;
+        if (t < 0) break;
+        const int64_t c = t / p.heads;
+        const int64_t head = t - c * p.heads;
+        const int64_t t0 = c * C;
+        const int nvalid = static_cast<int>(p.N - t0 < C ? p.N - t0 : C);
+        int nv = nvalid - wg * 32;                            // valid rows of this warp
+        nv = nv < 0 ? 0 : (nv > 32 ? 32 : nv);
+
+        float qv[E];
+        if (owns) {
+            load_vals<E>(reinterpret_cast<const Tin *>(gs + T::g_q) + lane * E, qv);
+        } else {
+#pragma unroll
+            for (int e = 0; e < E; ++e) qv[e] = 0.f;
+        }
+
+        // 1. scores (lane = dims, then transposed to lane = token).  The row
+        //    loops that need no register-held V stay rolled: the code of all
+        //    warps must fit the SM's instruction cache.
+        const Tin *Kw = reinterpret_cast<const Tin *>(stage) + size_t(wg) * 32 * D + lane * E;
+        const Tin *Vw = reinterpret_cast<const Tin *>(stage + T::half_bytes) + size_t(wg) * 32 * D +
+                        lane * E;
+        float s = -INFINITY;
+#pragma unroll 1
+        for (int quarter = 0; quarter < 4; ++quarter) {
+            float x[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int r = quarter * 8 + i;
+                x[i] = 0.f;
+                if (owns && r < nv) {
+                    RawRow<E> kr;
+                    lds_row<E>(Kw + size_t(r) * D, kr);
+                    float kf[E];
+                    unpack_row<E>(kr, kf);
+                    float acc = qv[0] * kf[0];
+#pragma unroll
+                    for (int e = 1; e < E; ++e) acc = fmaf(qv[e], kf[e], acc);
+                    x[i] = acc;
+                }
+            }
+            const float sr = transpose_sum8(x, lane);
+            if ((lane >> 3) == quarter) s = sr;
+        }
+        if (lane >= nv) s = -INFINITY;
+
+        // 2. warp aggregate (m_w, u_w, w_w) relative to the warp's maximum,
+        //    V read from the stage
+        const float mw = warp_max(s);
+        const float b = (s == -INFINITY) ? 0.f : exp_rel(s, mw);
+        const float ww = warp_sum(b);
+        {
+            float u[E];
+#pragma unroll
+            for (int e = 0; e < E; ++e) u[e] = 0.f;
+#pragma unroll 4
+            for (int r = 0; r < nv; ++r) {
+                const float br = __shfl_sync(kFull, b, r);
+                float v[E];
+                if (owns) {
+                    load_vals<E>(Vw + size_t(r) * D, v);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < E; ++e) v[e] = 0.f;
+                }
+#pragma unroll
+                for (int e = 0; e < E; ++e) u[e] = fmaf(br, v[e], u[e]);
+            }
+            write_state<D>(wst + (size_t(par) * kPipeComputeWarps + wg) * SS, mw, u, ww, lane);
+        }
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(aggb);
+
+        // V rows into registers (for the rescan); then hand the stage back
+        RawRow<E> vr[32];
+#pragma unroll
+        for (int r = 0; r < 32; ++r) {
+#pragma unroll
+            for (int k = 0; k < (E == 4 ? 2 : 1); ++k) vr[r].w[k] = 0u;
+            if (owns && r < nv) lds_row<E>(Vw + size_t(r) * D, vr[r]);
+        }
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(empty);
+
+        // 3. warp 0 publishes the chunk aggregate for successors' look-backs
+        //    (its wait for the carry would otherwise be idle); the carry warp
+        //    may already have published the inclusive prefix, which wins
+        if (wg == 0 && c > 0) {
+            const int64_t chunk = head * p.chunks_per_head + c;
+            if (chunk != p.fault_chunk && compute_wait(aggb, par, group_limit)) {
+                float am, aw, au[E];
+                chunk_aggregate<D>(wst + size_t(par) * kPipeComputeWarps * SS, am, au, aw, lane);
+                write_state<D>(p.states + size_t(chunk) * 2 * SS, am, au, aw, lane);
+                publish_agg_if_none(p.flags + chunk, lane);
+            }
+        }
+
+        // 4. wait for this warp's carry
+        if (!compute_wait(carryb, par, group_limit)) {
+            if (lane == 0) atomicOr(p.status, STATUS_LOAD_TIMEOUT);
+            break;
+        }
+        if (*fail) continue;
+
+        // 5. rescan from the carry, V from registers, and write O
+        if (nv > 0) {
+            float rm, rw, u[E];
+            read_state_smem<D>(cst + wg * SS, rm, u, rw, lane);
+            // scalar recurrences across lanes (lane = token)
+            float M = s;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const float y = __shfl_up_sync(kFull, M, off);
+                if (lane >= off) M = fmaxf(M, y);
+            }
+            M = fmaxf(M, rm);
+            float Mp = __shfl_up_sync(kFull, M, 1);
+            if (lane == 0) Mp = rm;
+            const float alpha = exp_rel(Mp, M);
+            const float beta = (s == -INFINITY) ? 0.f : exp_rel(s, M);
+            float A = alpha, Bc = beta;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const float Ap = __shfl_up_sync(kFull, A, off);
+                const float Bp = __shfl_up_sync(kFull, Bc, off);
+                if (lane >= off) {
+                    Bc = fmaf(A, Bp, Bc);
+                    A *= Ap;
+                }
+            }
+            const float wt = fmaf(A, rw, Bc);
+            const float rcp = (s == -INFINITY) ? 0.f : __frcp_rn(wt);
+            cf[lane] = make_float4(alpha, beta, rcp, 0.f);   // .w: the zero for unpack_row_late
+            __syncwarp();
+            Tout *orow = static_cast<Tout *>(p.O) + size_t(head * p.N + t0 + wg * 32) * D + lane * E;
+            // Rows in blocks of kRescanBlock: the block body is unrolled (V
+            // stays in registers under static names), the blocks are not, and
+            // the register-held rows shift down by one block after each (a
+            // few moves, for a loop body that fits the instruction cache).
+#pragma unroll 1
+            for (int rb = 0; rb < nv; rb += kRescanBlock) {
+#pragma unroll
+                for (int i = 0; i < kRescanBlock; ++i) {
+                    const int r = rb + i;
+                    if (r >= nv) break;
+                    const float4 k = cf[r];
+                    float v[E], o[E];
+                    unpack_row_late<E>(vr[i], __float_as_uint(k.w), v);
+                    if (k.x != 1.0f) {
+#pragma unroll
+                        for (int e = 0; e < E; ++e) u[e] *= k.x;
+                    }
+#pragma unroll
+                    for (int e = 0; e < E; ++e) {
+                        u[e] = fmaf(k.y, v[e], u[e]);
+                        o[e] = u[e] * k.z;
+                    }
+                    if (owns) store_vals<E>(orow + size_t(r) * D, o);
+                }
+#pragma unroll
+                for (int i = 0; i + kRescanBlock < 32; ++i) vr[i] = vr[i + kRescanBlock];
+            }
+            __syncwarp();
+        }
+    }
+}
+
+}  // namespace aaren
