@@ -42,17 +42,21 @@ sys.path.insert(0, ROOT)
 
 FALLBACK_HBM_GBS = 6400.0
 CPU_SAMPLE_TOKENS = 1 << 18      # per head, cpu_baseline leg
+CPU_SAMPLE_MIN_S = 1.0           # cpu_baseline: repeat the sample until this much wall time
+CPU_SAMPLE_MAX_PASSES = 12
 REF_STEP_TOKENS = 1 << 16        # per head, --impl reference steps
+METRIC = "Aaren scan tokens/s and achieved HBM GB/s (% of B300 peak), 1 GPU"
 
 
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="long", choices=["tiny", "bf16_4k", "stress", "long"])
     ap.add_argument("--heads", type=int, default=0, help="override H (profiling small cases)")
+    ap.add_argument("--tokens", type=int, default=0, help="override N (profiling small cases)")
     ap.add_argument("--out-dtype", default="", choices=["", "bf16", "f32"])
     return ap.parse_args()
 
@@ -67,8 +71,9 @@ def dist_env():
 def workload(args):
     from attention_prefix_scan_02_b300 import inputs
     wl = inputs.WORKLOADS[args.workload]
-    if args.heads:
-        wl = inputs.custom(wl.B, args.heads, wl.N, wl.d, wl.dtype, wl.seed, wl.kind, wl.name)
+    if args.heads or args.tokens:
+        wl = inputs.custom(wl.B, args.heads or wl.H, args.tokens or wl.N, wl.d, wl.dtype, wl.seed,
+                           wl.kind, wl.name if not args.tokens else f"{wl.name}_N{args.tokens}")
     return wl
 
 
@@ -94,7 +99,10 @@ def kernel_source_hash():
 
 def profiled_traffic(wl, out):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel source for this workload; else None."""
+    on the current kernel source with this head size, dtype and output type;
+    else None.  The capture is of a shorter sequence (the full launch is too
+    large for a multi-pass capture); its bytes per head-token are scaled to
+    this launch's head-tokens."""
     path = os.path.join(ROOT, "profiles", "scan_long_bf16_traffic.json")
     try:
         with open(path) as f:
@@ -103,10 +111,10 @@ def profiled_traffic(wl, out):
         return None
     if rec.get("kernel_source_sha") != kernel_source_hash():
         return None
-    if rec.get("workload") != wl.name or rec.get("out_dtype") != out:
+    if (rec.get("d") != wl.d or rec.get("in_dtype") != wl.dtype or rec.get("out_dtype") != out):
         return None
-    per_head = rec.get("dram_bytes_per_head")
-    return None if per_head is None else int(per_head * wl.heads)
+    per_token = rec.get("dram_bytes_per_head_token")
+    return None if per_token is None else int(per_token * wl.heads * wl.N)
 
 
 def measured_peak():
@@ -119,7 +127,11 @@ def measured_peak():
 
 
 class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi clock and throttle-reason samples every 20 ms; summary()
+    keeps the samples taken inside [begin, end] (host wall clock), the timed
+    region (or, when it is shorter than the sampling period, the samples
+    nearest to it)."""
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -127,6 +139,8 @@ class ClockSampler:
         self.gpu = gpu_index
         self.proc = None
         self.path = None
+        self.begin = None
+        self.end = None
 
     def __enter__(self):
         try:
@@ -135,7 +149,7 @@ class ClockSampler:
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=self.fh, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
@@ -151,6 +165,7 @@ class ClockSampler:
             self.fh.close()
 
     def summary(self):
+        import datetime
         if self.proc is None or self.path is None:
             return None
         rows = []
@@ -160,22 +175,31 @@ class ClockSampler:
                 if len(parts) < 9:
                     continue
                 try:
-                    rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+                    ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                    rows.append((ts, float(parts[1]), float(parts[2]), parts[5:9]))
                 except ValueError:
                     continue
         os.unlink(self.path)
         if not rows:
             return None
+        inside = [r for r in rows if self.begin is not None and self.begin <= r[0] <= self.end]
+        where = "inside the timed region"
+        if not inside and self.begin is not None:
+            mid = 0.5 * (self.begin + self.end)
+            inside = sorted(rows, key=lambda r: abs(r[0] - mid))[:2]
+            where = "nearest to the timed region (shorter than the sampling period)"
+        rows = inside or rows
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r) if v == "Active"})
-        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
-                "reasons": reasons, "samples": len(rows)}
+        reasons = sorted({names[i] for _, _, _, r in rows for i, v in enumerate(r) if v == "Active"})
+        return {"sm_mhz": statistics.median(r[1] for r in rows), "sm_max_mhz": max(r[2] for r in rows),
+                "reasons": reasons, "samples": len(rows), "samples_taken": where}
 
 
-def cpu_oracle_rate(wl, tokens_per_head, threads):
+def cpu_oracle_rate(wl, tokens_per_head, threads, min_s=0.0):
     """Time the float64 oracle (as it stands) over `tokens_per_head` leading
-    tokens of every head, heads spread over `threads` host threads.  Inputs
-    are drawn before the clock starts.  Returns (head-tokens/s, seconds)."""
+    tokens of every head, heads spread over `threads` host threads, repeating
+    the pass until `min_s` seconds have elapsed.  Inputs are drawn before the
+    clock starts.  Returns (head-tokens/s, seconds, tokens per head, passes)."""
     from concurrent.futures import ThreadPoolExecutor
 
     import oracle
@@ -188,11 +212,16 @@ def cpu_oracle_rate(wl, tokens_per_head, threads):
         q, K, V = x
         oracle.scan(q, K, V)      # O is computed and discarded
 
+    passes = 0
     t0 = time.perf_counter()
     with ThreadPoolExecutor(max_workers=threads) as ex:
-        list(ex.map(one, heads))
-    dt = time.perf_counter() - t0
-    return len(heads) * n / dt, dt, n
+        while True:
+            list(ex.map(one, heads))
+            passes += 1
+            dt = time.perf_counter() - t0
+            if dt >= min_s or passes >= CPU_SAMPLE_MAX_PASSES:
+                break
+    return passes * len(heads) * n / dt, dt, n, passes
 
 
 def host_cores():
@@ -212,13 +241,13 @@ def run_reference(args):
     threads = min(cores, wl.heads)
     rates = []
     for i in range(args.warmup + args.steps):
-        r, dt, n = cpu_oracle_rate(wl, REF_STEP_TOKENS, threads)
+        r, dt, n, _ = cpu_oracle_rate(wl, REF_STEP_TOKENS, threads)
         if i >= args.warmup:
             rates.append((r, dt))
     n = min(REF_STEP_TOKENS, wl.N)
     sample = f"each step: the first {n} tokens of all {wl.heads} heads ({n * wl.heads} head-tokens)"
     value = statistics.mean(r for r, _ in rates)
-    line = {"impl": "reference", "metric": "head-tokens/s of the Aaren prefix scan (and HBM GB/s)",
+    line = {"impl": "reference", "metric": METRIC,
             "value": value, "unit": "head-tokens/s", "n_gpus": args.gpus, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": 1e3 * statistics.mean(dt for _, dt in rates),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
@@ -256,10 +285,11 @@ def run_ours(args):
     if rank == 0:
         cores = host_cores()
         threads = min(cores, wl.heads)
-        rate, dt, n = cpu_oracle_rate(wl, CPU_SAMPLE_TOKENS, threads)
+        rate, dt, n, passes = cpu_oracle_rate(wl, CPU_SAMPLE_TOKENS, threads, CPU_SAMPLE_MIN_S)
         cpu = {"value": rate, "unit": "head-tokens/s", "cores": threads, "kind": "oracle",
-               "sample": f"the first {n} tokens of all {wl.heads} heads ({n * wl.heads} head-tokens, "
-                         f"{dt:.1f} s wall on {threads} threads)"}
+               "sample": f"the first {n} tokens of all {wl.heads} heads ({n * wl.heads} head-tokens), "
+                         f"{passes} passes, {dt:.1f} s wall on {threads} threads "
+                         f"(about {dt * threads:.0f} CPU-seconds)"}
 
     q, K, V = inputs.batch_inputs(wl, device="cuda")
     O = torch.empty(K.shape, dtype=out_t, device="cuda")
@@ -292,6 +322,7 @@ def run_ours(args):
     torch.cuda.synchronize()
     with ClockSampler(local) as clocks:
         time.sleep(0.3)
+        clocks.begin = time.time()
         t_start = torch.cuda.Event(enable_timing=True)
         t_end = torch.cuda.Event(enable_timing=True)
         t_start.record(stream)
@@ -303,6 +334,7 @@ def run_ours(args):
             ends[i].record(stream)
         t_end.record(stream)
         torch.cuda.synchronize()
+        clocks.end = time.time()
     if dist is not None:
         dist.barrier()
     status = binding.aaren_check()
@@ -368,7 +400,7 @@ def run_ours(args):
     achieved = alg_bytes / (mean_launch_ms * 1e-3) / 1e9
     traffic = profiled_traffic(wl, out)
     line = {
-        "metric": "head-tokens/s of the Aaren prefix scan (and HBM GB/s)",
+        "metric": METRIC,
         "value": world * tokens / (step_ms * 1e-3),
         "unit": "head-tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": warmup, "ms_per_step": step_ms,
@@ -379,7 +411,8 @@ def run_ours(args):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "algorithmic_bytes_per_launch": alg_bytes, "launch_ms": mean_launch_ms,
-                     "peak_source": peak_src, "kernel": "k_scan_fwd"},
+                     "peak_source": peak_src,
+                     "kernel": "k_scan_pipe" if wl.dtype == "bf16" else "k_scan_fwd"},
         "cpu_baseline": cpu,
         "e2e": e2e,
         "clocks": clocks.summary(),
