@@ -117,17 +117,26 @@ aaren_status_t launch_scan(const ScanParams &p, int64_t total_chunks, cudaStream
     return cudaGetLastError() == cudaSuccess ? AAREN_OK : AAREN_ERR_CUDA;
 }
 
-// Groups per block of the persistent bfloat16 kernel, per d: each group
-// holds one 128-token stage of K and V (64 KB at d = 128) and five warps.
+// Shape of the persistent bfloat16 kernel per d: groups (five warps each,
+// one 128-token chunk in flight) and stages in the block's pool (K, V and q
+// of one chunk each; 64 KB at d = 128).  A group holds a stage only from its
+// copy until its chunk is scored, so fewer stages than groups suffice.
 #ifndef AAREN_PIPE_GROUPS_D128
-#define AAREN_PIPE_GROUPS_D128 3
+#define AAREN_PIPE_GROUPS_D128 4
+#endif
+#ifndef AAREN_PIPE_STAGES_D128
+#define AAREN_PIPE_STAGES_D128 3
 #endif
 #ifndef AAREN_PIPE_GROUPS_D64
 #define AAREN_PIPE_GROUPS_D64 4
 #endif
+#ifndef AAREN_PIPE_STAGES_D64
+#define AAREN_PIPE_STAGES_D64 4
+#endif
 template <int D>
 struct PipeChoice {
     static constexpr int GROUPS = (D == 128) ? AAREN_PIPE_GROUPS_D128 : (D == 64 ? AAREN_PIPE_GROUPS_D64 : 4);
+    static constexpr int STAGES = (D == 128) ? AAREN_PIPE_STAGES_D128 : (D == 64 ? AAREN_PIPE_STAGES_D64 : 4);
 };
 
 int sm_count()
@@ -142,9 +151,9 @@ template <int D, typename Tout>
 aaren_status_t launch_pipe(const ScanParams &p, int64_t total_chunks, cudaStream_t st)
 {
     using PC = PipeChoice<D>;
-    using Tile = PipeTile<D, PC::GROUPS>;
+    using Tile = PipeTile<D, PC::GROUPS, PC::STAGES>;
     static std::atomic<unsigned long long> configured{0};
-    auto kern = k_scan_pipe<D, Tout, PC::GROUPS>;
+    auto kern = k_scan_pipe<D, Tout, PC::GROUPS, PC::STAGES>;
     if (allow_smem(kern, Tile::smem_bytes, configured) != cudaSuccess) return AAREN_ERR_CUDA;
     int per_sm = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, Tile::THREADS,

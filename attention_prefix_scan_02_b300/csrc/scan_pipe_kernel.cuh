@@ -56,42 +56,53 @@ constexpr int kPipeComputeWarps = 4;
 constexpr int kPipeGroupWarps = kPipeComputeWarps + 1;
 // predecessor states folded per memory round trip in the look-back
 #ifndef AAREN_PIPE_FOLD_BATCH
-#define AAREN_PIPE_FOLD_BATCH 12
+#define AAREN_PIPE_FOLD_BATCH 6
 #endif
 constexpr int kPipeFoldBatch = AAREN_PIPE_FOLD_BATCH;
 // rows per unrolled block of the rescan loop (32: fully unrolled)
 #ifndef AAREN_PIPE_RESCAN_BLOCK
-#define AAREN_PIPE_RESCAN_BLOCK 8
+#define AAREN_PIPE_RESCAN_BLOCK 4
 #endif
 constexpr int kRescanBlock = AAREN_PIPE_RESCAN_BLOCK;
 static_assert(32 % kRescanBlock == 0, "rescan blocks must tile the warp's 32 rows");
 
-template <int D, int GROUPS_>
+template <int D, int GROUPS_, int STAGES_>
 struct PipeTile {
     using Tin = __nv_bfloat16;
     static constexpr int GROUPS = GROUPS_;
+    static constexpr int STAGES = STAGES_;
     static constexpr int C = 32 * kPipeComputeWarps;   // tokens per chunk
     static constexpr int THREADS = 32 * kPipeGroupWarps * GROUPS;
     static constexpr int SS = StateLayout<D>::SS;
     static constexpr size_t half_bytes = size_t(C) * D * sizeof(Tin);   // K (or V) of a chunk
     static constexpr size_t q_bytes = size_t(D) * sizeof(Tin);
-    // per group: stage (K | V | q), warp aggregates (two sets), warp carries, rescan
-    // coefficients, ticket and failure word, four mbarriers
-    static constexpr size_t g_stage = 0;
-    static constexpr size_t g_q = g_stage + 2 * half_bytes;
-    static constexpr size_t g_wst = g_q + (q_bytes + 15) / 16 * 16;
-    // warp aggregates, double-buffered by chunk parity: compute warp 0 may
-    // still read a chunk's aggregates (to publish them) while the other warps
-    // write the next chunk's
+    // A stage of the block's pool: K | V | q of one chunk.
+    static constexpr size_t st_v = half_bytes;
+    static constexpr size_t st_q = 2 * half_bytes;
+    static constexpr size_t stage_bytes = st_q + (q_bytes + 15) / 16 * 16;
+    // Per group: warp aggregates (two sets, by chunk parity: compute warp 0
+    // may still read a chunk's aggregates to publish them while the other
+    // warps write the next chunk's), warp carries, rescan coefficients, the
+    // group's current chunk (ticket, stage, fill parity), failure word and
+    // four mbarriers.
+    static constexpr size_t g_wst = 0;
     static constexpr size_t g_cst = g_wst + 2 * size_t(kPipeComputeWarps) * SS * sizeof(float);
     static constexpr size_t g_coef = g_cst + size_t(kPipeComputeWarps) * SS * sizeof(float);
     static constexpr size_t g_meta = g_coef + size_t(kPipeComputeWarps) * 32 * sizeof(float4);
     static constexpr size_t g_bars = g_meta + 16;
     static constexpr size_t group_bytes = g_bars + 4 * sizeof(uint64_t);
-    static constexpr size_t smem_bytes = size_t(GROUPS) * group_bytes;
-    static_assert(half_bytes % 16 == 0 && g_wst % 16 == 0 && g_cst % 16 == 0 && g_coef % 16 == 0 &&
-                      g_meta % 16 == 0 && group_bytes % 16 == 0,
+    // Block: the stages, the groups, then the pool's free mask, the stages'
+    // fill counters and their "full" mbarriers.
+    static constexpr size_t group_off = size_t(STAGES) * stage_bytes;
+    static constexpr size_t pool_off = group_off + size_t(GROUPS) * group_bytes;
+    static constexpr size_t fills_off = pool_off + 16;
+    static constexpr size_t full_off = fills_off + (size_t(STAGES) * 4 + 7) / 8 * 8;
+    static constexpr size_t smem_bytes = full_off + size_t(STAGES) * sizeof(uint64_t);
+    static_assert(half_bytes % 16 == 0 && stage_bytes % 16 == 0 && g_cst % 16 == 0 &&
+                      g_coef % 16 == 0 && g_meta % 16 == 0 && group_bytes % 16 == 0 &&
+                      group_off % 16 == 0 && full_off % 8 == 0,
                   "shared-memory regions must stay aligned");
+    static_assert(STAGES >= 1 && STAGES <= 32, "the pool's free mask is one word");
     static_assert(smem_bytes <= 227 * 1024, "stages do not fit in shared memory");
 };
 
@@ -208,41 +219,54 @@ __device__ __forceinline__ bool compute_wait(uint64_t *bar, unsigned parity, int
     return AAREN_PIPE_SPIN_WAIT ? wait_bar_spin(bar, parity, limit_ns) : wait_bar(bar, parity, limit_ns);
 }
 
-template <int D, typename Tout, int GROUPS>
-__global__ void __launch_bounds__(PipeTile<D, GROUPS>::THREADS, 1)
+template <int D, typename Tout, int GROUPS, int STAGES>
+__global__ void __launch_bounds__(PipeTile<D, GROUPS, STAGES>::THREADS, 1)
     k_scan_pipe(const ScanParams p, const int64_t total_chunks)
 {
     using Tin = __nv_bfloat16;
     using L = VLayout<D>;
-    using T = PipeTile<D, GROUPS>;
+    using T = PipeTile<D, GROUPS, STAGES>;
     constexpr int E = L::E;
     constexpr int C = T::C;
     constexpr int SS = T::SS;
+    constexpr int WS = kPipeComputeWarps * SS;   // floats of one set of warp states
 
     extern __shared__ __align__(128) unsigned char smem[];
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int g = warp / kPipeGroupWarps;        // group
     const int role = warp % kPipeGroupWarps;     // 0..3 compute warp, 4 carry warp
-    unsigned char *gs = smem + size_t(g) * T::group_bytes;
-    unsigned char *stage = gs + T::g_stage;
-    float *wst = reinterpret_cast<float *>(gs + T::g_wst);
-    float *cst = reinterpret_cast<float *>(gs + T::g_cst);
-    volatile long long *meta = reinterpret_cast<volatile long long *>(gs + T::g_meta);
-    volatile int *fail = reinterpret_cast<volatile int *>(gs + T::g_meta + 8);
-    uint64_t *full = reinterpret_cast<uint64_t *>(gs + T::g_bars);   // stage loaded (1 + bytes)
-    uint64_t *empty = full + 1;                                       // stage read (4 warps)
-    uint64_t *aggb = full + 2;                                        // warp aggregates written (4)
-    uint64_t *carryb = full + 3;                                      // carries written (1)
+    unsigned char *gs = smem + T::group_off + size_t(g) * T::group_bytes;
+    float *wst = reinterpret_cast<float *>(gs + T::g_wst);   // [2][4][SS]
+    float *cst = reinterpret_cast<float *>(gs + T::g_cst);   // [4][SS]
+    // the group's current chunk: ticket, pool stage, parity of that stage's fill
+    volatile long long *meta_t = reinterpret_cast<volatile long long *>(gs + T::g_meta);
+    volatile int *meta_s = reinterpret_cast<volatile int *>(gs + T::g_meta + 8);
+    volatile int *fail = reinterpret_cast<volatile int *>(gs + T::g_meta + 12);
+    uint64_t *gbars = reinterpret_cast<uint64_t *>(gs + T::g_bars);
+    uint64_t *metab = gbars + 0;    // the group's next chunk is known (carry warp)
+    uint64_t *empty = gbars + 1;    // the chunk's stage has been read (4 compute warps)
+    uint64_t *aggb = gbars + 2;     // warp aggregates written (4 compute warps)
+    uint64_t *carryb = gbars + 3;   // carries written (carry warp)
+    unsigned *pool = reinterpret_cast<unsigned *>(smem + T::pool_off);          // free stages
+    unsigned *fills = reinterpret_cast<unsigned *>(smem + T::fills_off);        // per stage
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + T::full_off);          // per stage
     const bool owns = (L::LANES == 32 || lane < L::LANES);
 
+    if (threadIdx.x == 0) {
+        *pool = (STAGES == 32) ? 0xffffffffu : ((1u << STAGES) - 1u);
+        for (int st = 0; st < STAGES; ++st) {
+            fills[st] = 0;
+            ptx::mbar_init(full + st, 1);
+        }
+    }
     if (role == kPipeComputeWarps && lane == 0) {
-        ptx::mbar_init(full, 1);
+        ptx::mbar_init(metab, 1);
         ptx::mbar_init(empty, kPipeComputeWarps);
         ptx::mbar_init(aggb, kPipeComputeWarps);
         ptx::mbar_init(carryb, 1);
-        ptx::fence_barrier_init();
     }
+    if (threadIdx.x == 0) ptx::fence_barrier_init();
     __syncthreads();
     // waits on the group's own barriers may legitimately last as long as a
     // look-back wait, so they get a wider limit
@@ -251,50 +275,84 @@ __global__ void __launch_bounds__(PipeTile<D, GROUPS>::THREADS, 1)
     if (role == kPipeComputeWarps) {
         // ------------------------------------------------------------ carry warp
         const uint64_t pol = ptx::policy_evict_first();
-        bool exhausted = false;      // a stop ticket was posted
-        bool pending = false;        // a copy was issued whose phase was not yet consumed
-        // Take the group's next ticket into the (free) stage and start its copy.
-        // Returns false when the stage did not come free in time.
-        auto issue = [&](int64_t it) -> bool {
+        int held = -1;                // stage with a copy this warp issued (its chunk not yet aggregated)
+        unsigned held_par = 0;
+        // Claim a free stage of the block's pool, take the group's next
+        // ticket and start the chunk's copies; or post a stop.  False when no
+        // stage came free in time.
+        auto issue = [&]() -> bool {
             long long t = kTicketStop;
+            int st = -1;
+            unsigned par = 0;
             int ok = 1;
             if (lane == 0) {
-                ok = wait_bar(empty, static_cast<unsigned>(it & 1) ^ 1u, group_limit) ? 1 : 0;
+                const uint64_t t_start = ptx::globaltimer();
+                for (unsigned polls = 0;; ++polls) {
+                    const unsigned m = *reinterpret_cast<volatile unsigned *>(pool);
+                    if (m != 0) {
+                        const int cand = __ffs(m) - 1;
+                        if (atomicAnd(pool, ~(1u << cand)) & (1u << cand)) {
+                            st = cand;
+                            break;
+                        }
+                        continue;
+                    }
+                    if (polls >= kMinWaitPolls &&
+                        int64_t(ptx::globaltimer() - t_start) > group_limit) {
+                        ok = 0;
+                        break;
+                    }
+                    __nanosleep(64);
+                }
                 if (ok) {
+                    __threadfence_block();
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                     t = static_cast<long long>(atomicAdd(p.ticket, 1u));
-                    if (t >= total_chunks) t = kTicketStop;
-                    *meta = t;
-                    if (t < 0) {
-                        ptx::mbar_arrive(full);
-                    } else {
+                    if (t >= total_chunks) {
+                        t = kTicketStop;
+                        atomicOr(pool, 1u << st);   // nothing to load: give the stage back
+                        st = -1;
+                    }
+                    if (st >= 0) {
+                        par = fills[st] & 1u;
+                        fills[st] = fills[st] + 1;
+                    }
+                    *meta_t = t;
+                    *meta_s = st | static_cast<int>(par << 8);
+                    if (t >= 0) {
                         const int64_t c = t / p.heads;
                         const int64_t head = t - c * p.heads;
                         const int64_t t0 = c * C;
                         const int nvalid = static_cast<int>(p.N - t0 < C ? p.N - t0 : C);
                         const unsigned bytes = static_cast<unsigned>(nvalid) * D * sizeof(Tin);
                         const int64_t row0 = head * p.N + t0;
-                        ptx::mbar_arrive_expect_tx(full, 2 * bytes + unsigned(T::q_bytes));
-                        ptx::bulk_g2s(stage, static_cast<const Tin *>(p.K) + row0 * D, bytes, full, pol);
-                        ptx::bulk_g2s(stage + T::half_bytes, static_cast<const Tin *>(p.V) + row0 * D,
-                                      bytes, full, pol);
-                        ptx::bulk_g2s(gs + T::g_q, static_cast<const Tin *>(p.q) + head * D,
-                                      unsigned(T::q_bytes), full, pol);
+                        unsigned char *stage = smem + size_t(st) * T::stage_bytes;
+                        ptx::mbar_arrive_expect_tx(full + st, 2 * bytes + unsigned(T::q_bytes));
+                        ptx::bulk_g2s(stage, static_cast<const Tin *>(p.K) + row0 * D, bytes, full + st,
+                                      pol);
+                        ptx::bulk_g2s(stage + T::st_v, static_cast<const Tin *>(p.V) + row0 * D, bytes,
+                                      full + st, pol);
+                        ptx::bulk_g2s(stage + T::st_q, static_cast<const Tin *>(p.q) + head * D,
+                                      unsigned(T::q_bytes), full + st, pol);
                     }
+                    ptx::mbar_arrive(metab);
                 }
             }
             ok = __shfl_sync(kFull, ok, 0);
             t = __shfl_sync(kFull, t, 0);
-            if (ok) {
-                exhausted = (t < 0);
-                pending = (t >= 0);
+            st = __shfl_sync(kFull, st, 0);
+            par = __shfl_sync(kFull, par, 0);
+            if (ok && t >= 0) {
+                held = st;
+                held_par = par;
             }
-            return ok != 0;
+            return ok != 0 && t >= 0;
         };
 
-        bool ok = issue(0);
+        bool live = issue();
         int64_t it = 0;
-        for (; ok && !exhausted; ++it) {
-            const long long t = __shfl_sync(kFull, lane == 0 ? *meta : 0ll, 0);
+        for (; live; ++it) {
+            const long long t = __shfl_sync(kFull, lane == 0 ? *meta_t : 0ll, 0);
             const unsigned par = static_cast<unsigned>(it & 1);
             const int64_t c = t / p.heads;
             const int64_t head = t - c * p.heads;
@@ -321,9 +379,9 @@ __global__ void __launch_bounds__(PipeTile<D, GROUPS>::THREADS, 1)
                 if (lane == 0) atomicOr(p.status, STATUS_LOAD_TIMEOUT);
                 break;   // the compute warps stopped
             }
-            pending = false;   // the compute warps have consumed the copy
+            held = -1;   // the compute warps have consumed the copy
             float am, aw, au[E];
-            const float *wst_it = wst + size_t(par) * kPipeComputeWarps * SS;
+            const float *wst_it = wst + par * WS;
             chunk_aggregate<D>(wst_it, am, au, aw, lane);
             if (lb_ok) {
                 float im = am, iw = aw, iu[E];
@@ -369,12 +427,11 @@ __global__ void __launch_bounds__(PipeTile<D, GROUPS>::THREADS, 1)
                 if (lane == 0) ptx::mbar_arrive(carryb);
                 if (publish) publish_flag(my_flag, FLAG_POISON, lane);
             }
-            ok = issue(it + 1);
-            if (!ok && lane == 0) atomicOr(p.status, STATUS_LOAD_TIMEOUT);
+            live = issue();
         }
         // A copy this warp issued can still be in flight only if the compute
         // warps stopped early: wait for it before the block's memory goes.
-        if (pending && lane == 0) wait_bar(full, static_cast<unsigned>(it & 1), group_limit);
+        if (held >= 0 && lane == 0) wait_bar(full + held, held_par, group_limit);
         return;
     }
 
@@ -383,12 +440,20 @@ __global__ void __launch_bounds__(PipeTile<D, GROUPS>::THREADS, 1)
     float4 *cf = reinterpret_cast<float4 *>(gs + T::g_coef) + wg * 32;
     for (int64_t it = 0;; ++it) {
         const unsigned par = static_cast<unsigned>(it & 1);
-        if (!compute_wait(full, par, group_limit)) {
+        if (!compute_wait(metab, par, group_limit)) {
             if (lane == 0) atomicOr(p.status, STATUS_LOAD_TIMEOUT);
             break;
         }
-        const long long t = *meta;
+        const long long t = *meta_t;
         if (t < 0) break;
+        const int st_word = *meta_s;
+        const int st = st_word & 0xff;
+        const unsigned fill_par = static_cast<unsigned>(st_word >> 8) & 1u;
+        if (!compute_wait(full + st, fill_par, group_limit)) {
+            if (lane == 0) atomicOr(p.status, STATUS_LOAD_TIMEOUT);
+            break;
+        }
+        const unsigned char *stage = smem + size_t(st) * T::stage_bytes;
         const int64_t c = t / p.heads;
         const int64_t head = t - c * p.heads;
         const int64_t t0 = c * C;
@@ -398,7 +463,7 @@ __global__ void __launch_bounds__(PipeTile<D, GROUPS>::THREADS, 1)
 
         float qv[E];
         if (owns) {
-            load_vals<E>(reinterpret_cast<const Tin *>(gs + T::g_q) + lane * E, qv);
+            load_vals<E>(reinterpret_cast<const Tin *>(stage + T::st_q) + lane * E, qv);
         } else {
 #pragma unroll
             for (int e = 0; e < E; ++e) qv[e] = 0.f;
@@ -408,8 +473,7 @@ __global__ void __launch_bounds__(PipeTile<D, GROUPS>::THREADS, 1)
         //    loops that need no register-held V stay rolled: the code of all
         //    warps must fit the SM's instruction cache.
         const Tin *Kw = reinterpret_cast<const Tin *>(stage) + size_t(wg) * 32 * D + lane * E;
-        const Tin *Vw = reinterpret_cast<const Tin *>(stage + T::half_bytes) + size_t(wg) * 32 * D +
-                        lane * E;
+        const Tin *Vw = reinterpret_cast<const Tin *>(stage + T::st_v) + size_t(wg) * 32 * D + lane * E;
         float s = -INFINITY;
 #pragma unroll 1
         for (int quarter = 0; quarter < 4; ++quarter) {
@@ -456,12 +520,13 @@ __global__ void __launch_bounds__(PipeTile<D, GROUPS>::THREADS, 1)
 #pragma unroll
                 for (int e = 0; e < E; ++e) u[e] = fmaf(br, v[e], u[e]);
             }
-            write_state<D>(wst + (size_t(par) * kPipeComputeWarps + wg) * SS, mw, u, ww, lane);
+            write_state<D>(wst + par * WS + wg * SS, mw, u, ww, lane);
         }
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(aggb);
 
-        // V rows into registers (for the rescan); then hand the stage back
+        // V rows into registers (for the rescan); then hand the stage back to
+        // the pool (compute warp 0, once all four warps are done with it)
         RawRow<E> vr[32];
 #pragma unroll
         for (int r = 0; r < 32; ++r) {
@@ -471,6 +536,17 @@ __global__ void __launch_bounds__(PipeTile<D, GROUPS>::THREADS, 1)
         }
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(empty);
+        if (wg == 0) {
+            if (lane == 0) {
+                if (wait_bar(empty, par, group_limit)) {
+                    __threadfence_block();
+                    atomicOr(pool, 1u << st);
+                } else {
+                    atomicOr(p.status, STATUS_LOAD_TIMEOUT);
+                }
+            }
+            __syncwarp();
+        }
 
         // 3. warp 0 publishes the chunk aggregate for successors' look-backs
         //    (its wait for the carry would otherwise be idle); the carry warp
@@ -479,7 +555,7 @@ __global__ void __launch_bounds__(PipeTile<D, GROUPS>::THREADS, 1)
             const int64_t chunk = head * p.chunks_per_head + c;
             if (chunk != p.fault_chunk && compute_wait(aggb, par, group_limit)) {
                 float am, aw, au[E];
-                chunk_aggregate<D>(wst + size_t(par) * kPipeComputeWarps * SS, am, au, aw, lane);
+                chunk_aggregate<D>(wst + par * WS, am, au, aw, lane);
                 write_state<D>(p.states + size_t(chunk) * 2 * SS, am, au, aw, lane);
                 publish_agg_if_none(p.flags + chunk, lane);
             }
