@@ -68,6 +68,25 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(x, dist, device):
+    """The largest of every rank's `x` (a step time); `dist` is
+    torch.distributed with an initialised process group, or None for one
+    rank.  Every rank gets the result."""
+    if dist is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank, world, step_ms):
+    """Units processed by all ranks per second, each rank doing the same
+    `units_per_rank` in a step of `step_ms` (the slowest rank's): weak
+    scaling, so the job's work grows with the number of ranks."""
+    return world * units_per_rank / (step_ms * 1e-3)
+
+
 def workload(args):
     from attention_prefix_scan_02_b300 import inputs
     wl = inputs.WORKLOADS[args.workload]
@@ -343,10 +362,7 @@ def run_ours(args):
     launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     mean_launch_ms = statistics.mean(launch_ms)
     step_ms = mean_launch_ms if flush is not None else t_start.elapsed_time(t_end) / args.steps
-    if dist is not None:
-        t = torch.tensor([step_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        step_ms = float(t.item())
+    step_ms = max_over_ranks(step_ms, dist, "cuda")
 
     # end to end through the C ABI with host buffers
     e2e = None
@@ -378,14 +394,11 @@ def run_ours(args):
         b.record(stream)
         torch.cuda.synchronize()
         e2e_ms = a.elapsed_time(b) / e2e_steps
-        if dist is not None:
-            t = torch.tensor([e2e_ms], device="cuda")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
+        e2e_ms = max_over_ranks(e2e_ms, dist, "cuda")
         if binding.aaren_check() != binding.AAREN_OK:
             raise SystemExit("device status error in the end-to-end leg")
         h2d = (hq.numel() + hK.numel() + hV.numel()) * in_b
-        e2e = {"value": world * tokens / (e2e_ms * 1e-3), "unit": "head-tokens/s",
+        e2e = {"value": whole_job_rate(tokens, world, e2e_ms), "unit": "head-tokens/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": hO.numel() * out_b,
                "ms_per_step": e2e_ms, "steps": e2e_steps,
                "path": "pinned host q,K,V -> device, aaren_scan_forward_ex, device O -> pinned host"}
@@ -401,7 +414,7 @@ def run_ours(args):
     traffic = profiled_traffic(wl, out)
     line = {
         "metric": METRIC,
-        "value": world * tokens / (step_ms * 1e-3),
+        "value": whole_job_rate(tokens, world, step_ms),
         "unit": "head-tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": warmup, "ms_per_step": step_ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
