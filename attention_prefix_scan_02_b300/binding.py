@@ -34,7 +34,7 @@ EXPORTS = (
     "aaren_scan_forward", "aaren_scan_forward_ex", "aaren_scan_workspace_bytes",
     "aaren_state_init", "aaren_step", "aaren_check", "aaren_status_string",
     "aaren_abi_version", "aaren_debug_set_fault", "aaren_scan_chunk_tokens",
-    "aaren_scan_forward_noalloc",
+    "aaren_scan_forward_noalloc", "aaren_scan_reduce", "aaren_reduce_workspace_bytes",
 )
 
 # size of the fixed device scratch of aaren_scan_forward_noalloc (include/aaren.h)
@@ -87,6 +87,11 @@ def load(path: str | None = None):
     lib.aaren_scan_chunk_tokens.restype = _i64
     lib.aaren_scan_forward_noalloc.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i32, _vp]
     lib.aaren_scan_forward_noalloc.restype = _i32
+    lib.aaren_scan_reduce.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i32,
+                                      _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
+    lib.aaren_scan_reduce.restype = _i32
+    lib.aaren_reduce_workspace_bytes.argtypes = [_i64, _i64, _i64, _i64]
+    lib.aaren_reduce_workspace_bytes.restype = ctypes.c_size_t
     if path is None:
         _lib = lib
     return lib
@@ -207,6 +212,37 @@ def aaren_scan_forward_noalloc(q, K, V, O, stream=None):
     return O
 
 
+def aaren_reduce_workspace_bytes(B: int, H: int, N: int, d: int) -> int:
+    return int(load().aaren_reduce_workspace_bytes(B, H, N, d))
+
+
+def aaren_scan_reduce(q, K, V, o_last=None, m_in=None, u_in=None, w_in=None, m_out=None,
+                      u_out=None, w_out=None, workspace=None, stream=None):
+    """Many-to-one output: o_last [B*H, d] = o_N of each head (or None), and
+    the final state (m_out, u_out, w_out) when given; no per-token output.
+    q [B,H,d], K/V [B,H,N,d]; optional starting state (m_in, u_in, w_in)."""
+    lib = load()
+    if K.dim() != 4 or tuple(V.shape) != tuple(K.shape):
+        raise ValueError("K and V must have the same shape [B, H, N, d]")
+    B, H, N, d = K.shape
+    if tuple(q.shape) != (B, H, d) or q.dtype != K.dtype or V.dtype != K.dtype:
+        raise ValueError("q must be [B, H, d] and share the dtype of K and V")
+    if o_last is not None and o_last.numel() != B * H * d:
+        raise ValueError("o_last must hold [B*H, d]")
+    _check_cuda(q, K, V, o_last, workspace)
+    _check_state(m_in, u_in, w_in, B * H, d)
+    _check_state(m_out, u_out, w_out, B * H, d)
+    code = dtype_code(K.dtype, o_last.dtype if o_last is not None else
+                      (torch.float32 if K.dtype == torch.float32 else torch.bfloat16))
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = lib.aaren_scan_reduce(
+        _ptr(q), _ptr(K), _ptr(V), _ptr(o_last), B, H, N, d, code,
+        _ptr(m_in), _ptr(u_in), _ptr(w_in), _ptr(m_out), _ptr(u_out), _ptr(w_out),
+        _ptr(workspace), ws_bytes, _stream_handle(stream))
+    _raise(rc, "aaren_scan_reduce")
+    return o_last
+
+
 def aaren_state_init(m, u, w, stream=None):
     """Identity state (-inf, 0, 0): m [n], u [n, d], w [n] (float32)."""
     n, d = u.shape
@@ -265,6 +301,30 @@ def scan_forward(q, K, V, out_dtype=None, init=None, return_state=False, workspa
         w_out = torch.empty(B * H, dtype=torch.float32, device=K.device)
     aaren_scan_forward_ex(q, K, V, O, m_in, u_in, w_in, m_out, u_out, w_out, workspace, stream)
     return (O, (m_out, u_out, w_out)) if return_state else O
+
+
+def scan_reduce(q, K, V, out_dtype=None, init=None, return_state=False, workspace=None,
+                stream=None):
+    """Allocate o_N [B, H, d] (and the final state when asked) and run
+    aaren_scan_reduce.  Returns o_N, or (o_N, (m, u, w))."""
+    out_dtype = out_dtype or K.dtype
+    B, H, N, d = K.shape
+    o = torch.empty(B, H, d, dtype=out_dtype, device=K.device)
+    m_in = u_in = w_in = None
+    if init is not None:
+        m_in, u_in, w_in = init
+    m_out = u_out = w_out = None
+    if return_state:
+        m_out = torch.empty(B * H, dtype=torch.float32, device=K.device)
+        u_out = torch.empty(B * H, d, dtype=torch.float32, device=K.device)
+        w_out = torch.empty(B * H, dtype=torch.float32, device=K.device)
+    aaren_scan_reduce(q, K, V, o, m_in, u_in, w_in, m_out, u_out, w_out, workspace, stream)
+    return (o, (m_out, u_out, w_out)) if return_state else o
+
+
+def new_reduce_workspace(B, H, N, d, device="cuda"):
+    nbytes = aaren_reduce_workspace_bytes(B, H, N, d)
+    return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
 
 
 def new_workspace(B, H, N, d, device="cuda"):

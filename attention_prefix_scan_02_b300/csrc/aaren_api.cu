@@ -13,6 +13,7 @@
 #include "common.cuh"
 #include "scan_kernel.cuh"
 #include "scan_pipe_kernel.cuh"
+#include "reduce_kernel.cuh"
 #include "step_kernel.cuh"
 
 namespace aaren {
@@ -242,6 +243,87 @@ aaren_status_t check_state(const float *m, const float *u, const float *w)
     return AAREN_OK;
 }
 
+// ---------------------------------------------------------------- reduce
+
+// Parts per head the workspace is sized for: at most 8192 part states in
+// all and at least kReduceMinSeg tokens per part.
+int64_t reduce_parts_max(int64_t BH, int64_t N)
+{
+    int64_t by_n = (N + kReduceMinSeg - 1) / kReduceMinSeg;
+    int64_t by_total = 8192 / (BH > 0 ? BH : 1);
+    int64_t P = by_n < by_total ? by_n : by_total;
+    return P < 1 ? 1 : P;
+}
+
+struct ReduceLayout {
+    size_t parts_off, bytes, zero_bytes;
+    int64_t P_max;
+};
+
+bool reduce_layout(int64_t BH, int64_t N, int64_t d, ReduceLayout *r)
+{
+    r->P_max = reduce_parts_max(BH, N);
+    int64_t states;
+    if (!mul_ok(BH, r->P_max, &states)) return false;
+    const size_t counts = ((size_t(BH) * 4 + 255) / 256) * 256;
+    r->parts_off = counts;
+    r->zero_bytes = counts;
+    r->bytes = counts + size_t(states) * size_t(d + 4) * sizeof(float);
+    return true;
+}
+
+template <int D, typename Tin, typename Tout>
+aaren_status_t launch_reduce(ReduceParams p, int64_t P_max, cudaStream_t st)
+{
+    auto kern = k_scan_reduce<D, Tin, Tout>;
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kReduceWarps * 32, 0) != cudaSuccess ||
+        per_sm < 1)
+        return AAREN_ERR_CUDA;
+    const int sms = sm_count();
+    if (sms <= 0) return AAREN_ERR_CUDA;
+    // one part per resident warp across the GPU (one wave), parts of equal length
+    const int64_t target = int64_t(sms) * per_sm * kReduceWarps;
+    int64_t P = (target + p.heads - 1) / p.heads;
+    if (P > P_max) P = P_max;
+    if (P < 1) P = 1;
+    int64_t seg = (p.N + P - 1) / P;
+    seg = ((seg + kReduceRows - 1) / kReduceRows) * kReduceRows;
+    if (seg < kReduceRows) seg = kReduceRows;
+    P = (p.N + seg - 1) / seg;
+    if (P < 1) P = 1;
+    p.P = P;
+    p.seg = seg;
+    const int64_t warps = p.heads * P;
+    const int64_t blocks = (warps + kReduceWarps - 1) / kReduceWarps;
+    if (blocks > INT_MAX) return AAREN_ERR_INVALID;
+    kern<<<unsigned(blocks), kReduceWarps * 32, 0, st>>>(p);
+    return cudaGetLastError() == cudaSuccess ? AAREN_OK : AAREN_ERR_CUDA;
+}
+
+template <int D>
+aaren_status_t dispatch_reduce_dtype(const ReduceParams &p, int64_t P_max, int32_t dtype, cudaStream_t st)
+{
+    switch (dtype) {
+    case AAREN_F32: return launch_reduce<D, float, float>(p, P_max, st);
+    case AAREN_BF16: return launch_reduce<D, __nv_bfloat16, __nv_bfloat16>(p, P_max, st);
+    case AAREN_BF16_F32OUT: return launch_reduce<D, __nv_bfloat16, float>(p, P_max, st);
+    default: return AAREN_ERR_UNSUPPORTED;
+    }
+}
+
+aaren_status_t dispatch_reduce(const ReduceParams &p, int64_t P_max, int64_t d, int32_t dtype,
+                               cudaStream_t st)
+{
+    switch (d) {
+    case 16: return dispatch_reduce_dtype<16>(p, P_max, dtype, st);
+    case 32: return dispatch_reduce_dtype<32>(p, P_max, dtype, st);
+    case 64: return dispatch_reduce_dtype<64>(p, P_max, dtype, st);
+    case 128: return dispatch_reduce_dtype<128>(p, P_max, dtype, st);
+    default: return AAREN_ERR_UNSUPPORTED;
+    }
+}
+
 }  // namespace
 }  // namespace aaren
 
@@ -334,6 +416,72 @@ aaren_status_t aaren_scan_forward_ex(const void *q, const void *K, const void *V
             p.wait_limit_ns = g_wait_limit_ns.load();
             rc = dispatch_scan(p, wl.total_chunks, d, dtype, st);
         }
+    }
+    if (owned && cudaFreeAsync(ws, st) != cudaSuccess && rc == AAREN_OK) rc = AAREN_ERR_CUDA;
+    return rc;
+}
+
+size_t aaren_reduce_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t d)
+{
+    if (!supported_d(d) || B < 0 || H < 0 || N < 0) return SIZE_MAX;
+    int64_t BH;
+    if (!mul_ok(B, H, &BH)) return SIZE_MAX;
+    if (BH == 0) return 0;
+    ReduceLayout r;
+    if (!reduce_layout(BH, N, d, &r)) return SIZE_MAX;
+    return r.bytes;
+}
+
+aaren_status_t aaren_scan_reduce(const void *q, const void *K, const void *V, void *o_last, int64_t B,
+                                 int64_t H, int64_t N, int64_t d, int32_t dtype, const float *m_in,
+                                 const float *u_in, const float *w_in, float *m_out, float *u_out,
+                                 float *w_out, void *workspace, size_t workspace_bytes, void *stream)
+{
+    if (!supported_dtype(dtype) || !supported_d(d)) return AAREN_ERR_UNSUPPORTED;
+    if (B < 0 || H < 0 || N < 0) return AAREN_ERR_INVALID;
+    if (check_state(m_in, u_in, w_in) != AAREN_OK) return AAREN_ERR_INVALID;
+    if (check_state(m_out, u_out, w_out) != AAREN_OK) return AAREN_ERR_INVALID;
+    int64_t BH, BHN, elems;
+    if (!mul_ok(B, H, &BH) || !mul_ok(BH, N, &BHN) || !mul_ok(BHN, d, &elems)) return AAREN_ERR_INVALID;
+    int64_t kv_bytes;
+    if (!mul_ok(elems, int64_t(in_elem_bytes(dtype)), &kv_bytes)) return AAREN_ERR_INVALID;
+    if (o_last == nullptr && m_out == nullptr) return AAREN_ERR_INVALID;   // nothing to compute
+    if (BH == 0) return AAREN_OK;
+    // o_N of an empty prefix is 0/0: it needs a starting state
+    if (N == 0 && o_last != nullptr && m_in == nullptr) return AAREN_ERR_INVALID;
+    if (q == nullptr || (N > 0 && (K == nullptr || V == nullptr))) return AAREN_ERR_INVALID;
+    if (!aligned(q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(o_last, 16))
+        return AAREN_ERR_INVALID;
+    if (o_last != nullptr && (overlaps(o_last, size_t(BH) * d * out_elem_bytes(dtype), K, size_t(kv_bytes)) ||
+                              overlaps(o_last, size_t(BH) * d * out_elem_bytes(dtype), V, size_t(kv_bytes))))
+        return AAREN_ERR_INVALID;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    ReduceLayout rl;
+    if (!reduce_layout(BH, N, d, &rl)) return AAREN_ERR_INVALID;
+    void *ws = workspace;
+    bool owned = false;
+    if (ws == nullptr) {
+        if (cudaMallocAsync(&ws, rl.bytes, st) != cudaSuccess) return AAREN_ERR_CUDA;
+        owned = true;
+    } else if (workspace_bytes < rl.bytes || !aligned(ws, 256)) {
+        return AAREN_ERR_WORKSPACE;
+    }
+    aaren_status_t rc = AAREN_OK;
+    if (cudaMemsetAsync(ws, 0, rl.zero_bytes, st) != cudaSuccess) {
+        rc = AAREN_ERR_CUDA;
+    } else {
+        char *base = static_cast<char *>(ws);
+        ReduceParams p;
+        p.q = q; p.K = K; p.V = V; p.o_last = o_last;
+        p.m_in = m_in; p.u_in = u_in; p.w_in = w_in;
+        p.m_out = m_out; p.u_out = u_out; p.w_out = w_out;
+        p.counts = reinterpret_cast<unsigned *>(base);
+        p.parts = reinterpret_cast<float *>(base + rl.parts_off);
+        p.N = N;
+        p.heads = BH;
+        p.P = 1;
+        p.seg = kReduceRows;
+        rc = dispatch_reduce(p, rl.P_max, d, dtype, st);
     }
     if (owned && cudaFreeAsync(ws, st) != cudaSuccess && rc == AAREN_OK) rc = AAREN_ERR_CUDA;
     return rc;

@@ -58,6 +58,9 @@ def parse():
     ap.add_argument("--heads", type=int, default=0, help="override H (profiling small cases)")
     ap.add_argument("--tokens", type=int, default=0, help="override N (profiling small cases)")
     ap.add_argument("--out-dtype", default="", choices=["", "bf16", "f32"])
+    ap.add_argument("--op", default="scan", choices=["scan", "reduce"],
+                    help="scan: every prefix output (the headline); reduce: the many-to-one "
+                         "form (o_N and the final state only)")
     return ap.parse_args()
 
 
@@ -311,21 +314,29 @@ def run_ours(args):
                          f"(about {dt * threads:.0f} CPU-seconds)"}
 
     q, K, V = inputs.batch_inputs(wl, device="cuda")
-    O = torch.empty(K.shape, dtype=out_t, device="cuda")
-    ws = binding.new_workspace(wl.B, wl.H, wl.N, wl.d)
+    reduce = args.op == "reduce"
+    O = torch.empty((wl.B, wl.H, wl.d) if reduce else K.shape, dtype=out_t, device="cuda")
+    ws = (binding.new_reduce_workspace if reduce else binding.new_workspace)(wl.B, wl.H, wl.N, wl.d)
     stream = torch.cuda.current_stream()
     in_b = 2 if wl.dtype == "bf16" else 4
     out_b = 2 if out == "bf16" else 4
     elems = wl.heads * wl.N * wl.d
-    alg_bytes = elems * (2 * in_b + out_b)          # K, V read once + O written once
+    # algorithmic bytes: K, V read once (+ O written once for the scan)
+    alg_bytes = elems * (2 * in_b + (0 if reduce else out_b))
     tokens = wl.heads * wl.N
     flush = None
     if elems * 2 * in_b < (1 << 28):                # small workloads sit in L2: flush it
         flush = torch.empty(2 * torch.cuda.get_device_properties(0).L2_cache_size // 4 + 1,
                             dtype=torch.float32, device="cuda")
 
+    def call(q, K, V, O):
+        if reduce:
+            binding.aaren_scan_reduce(q, K, V, O, workspace=ws, stream=stream)
+        else:
+            binding.aaren_scan_forward_ex(q, K, V, O, workspace=ws, stream=stream)
+
     def step():
-        binding.aaren_scan_forward_ex(q, K, V, O, workspace=ws, stream=stream)
+        call(q, K, V, O)
 
     for _ in range(warmup):
         if flush is not None:
@@ -379,7 +390,7 @@ def run_ours(args):
             dq.copy_(hq, non_blocking=True)
             dK.copy_(hK, non_blocking=True)
             dV.copy_(hV, non_blocking=True)
-            binding.aaren_scan_forward_ex(dq, dK, dV, dO, workspace=ws, stream=stream)
+            call(dq, dK, dV, dO)
             hO.copy_(dO, non_blocking=True)
 
         e2e_step()
@@ -401,7 +412,9 @@ def run_ours(args):
         e2e = {"value": whole_job_rate(tokens, world, e2e_ms), "unit": "head-tokens/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": hO.numel() * out_b,
                "ms_per_step": e2e_ms, "steps": e2e_steps,
-               "path": "pinned host q,K,V -> device, aaren_scan_forward_ex, device O -> pinned host"}
+               "path": ("pinned host q,K,V -> device, aaren_scan_reduce, device o_N -> pinned host"
+                        if reduce else
+                        "pinned host q,K,V -> device, aaren_scan_forward_ex, device O -> pinned host")}
         del hq, hK, hV, hO
 
     if rank != 0:
@@ -411,7 +424,7 @@ def run_ours(args):
 
     peak, peak_src = measured_peak()
     achieved = alg_bytes / (mean_launch_ms * 1e-3) / 1e9
-    traffic = profiled_traffic(wl, out)
+    traffic = None if reduce else profiled_traffic(wl, out)
     line = {
         "metric": METRIC,
         "value": whole_job_rate(tokens, world, step_ms),
@@ -419,13 +432,14 @@ def run_ours(args):
         "n_gpus": world, "steps": args.steps, "warmup": warmup, "ms_per_step": step_ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32", "data": "synthetic",
-        "config": describe(wl, out),
+        "config": dict(describe(wl, out), op=args.op),
         "gpu_launches": args.steps,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "algorithmic_bytes_per_launch": alg_bytes, "launch_ms": mean_launch_ms,
                      "peak_source": peak_src,
-                     "kernel": "k_scan_pipe" if wl.dtype == "bf16" else "k_scan_fwd"},
+                     "kernel": "k_scan_reduce" if reduce else
+                               ("k_scan_pipe" if wl.dtype == "bf16" else "k_scan_fwd")},
         "cpu_baseline": cpu,
         "e2e": e2e,
         "clocks": clocks.summary(),

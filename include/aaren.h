@@ -120,6 +120,45 @@ aaren_status_t aaren_scan_forward_ex(const void *q, const void *K,
 size_t aaren_scan_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t d);
 
 /*
+ * aaren_scan_reduce -- the many-to-one output: for every head only the last
+ * output o_N = sum_{i<=N} e^{s_i} v_i / sum_{i<=N} e^{s_i} and, optionally,
+ * the final state (m, u, w); no per-token output is written, so K and V are
+ * the only large traffic ("Attention as an RNN" review, "Proposed method":
+ * attention as a many-to-one RNN; "Self-attention Does Not Need O(n^2)
+ * Memory" review, section 2 "Algorithm": the single-query running sums).
+ * Each head's tokens are reduced in independent parts that are combined at
+ * the end (the state operator is associative and commutative), so nothing
+ * waits on a neighbouring part.
+ *   q  [B,H,d], K, V [B,H,N,d]   as for aaren_scan_forward (input type)
+ *   o_last [B*H,d]   o_N of each head (output type), written; NULL = not
+ *        computed.  Must not overlap K or V.
+ *   m_in, u_in, w_in   optional starting state (all NULL = identity), read
+ *   m_out, u_out, w_out   optional final state (all NULL = not written)
+ *   workspace, workspace_bytes   device scratch of at least
+ *        aaren_reduce_workspace_bytes(B,H,N,d) bytes, 256-byte aligned; NULL
+ *        = taken from the stream-ordered allocator for this call.  Contents
+ *        need no initialisation; calls in flight at once must not share it.
+ * At least one of o_last and the final state must be requested.  N = 0:
+ * the final state is the starting state, and o_last needs a starting state
+ * (the empty prefix has no output).  The result does not depend on the
+ * launch shape chosen for the device beyond float32 rounding (parts are
+ * combined in token order).
+ * Errors: AAREN_ERR_INVALID, AAREN_ERR_UNSUPPORTED, AAREN_ERR_CUDA,
+ * AAREN_ERR_WORKSPACE.
+ */
+aaren_status_t aaren_scan_reduce(const void *q, const void *K, const void *V,
+                                 void *o_last, int64_t B, int64_t H,
+                                 int64_t N, int64_t d, int32_t dtype,
+                                 const float *m_in, const float *u_in,
+                                 const float *w_in, float *m_out,
+                                 float *u_out, float *w_out, void *workspace,
+                                 size_t workspace_bytes, void *stream);
+
+/* Bytes of workspace aaren_scan_reduce needs for this shape (0 when
+ * B*H = 0; SIZE_MAX when d is unsupported or the shape overflows). */
+size_t aaren_reduce_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t d);
+
+/*
  * aaren_state_init -- set n states to the identity (m = -inf, u = 0, w = 0),
  * the state of an empty prefix, before the first aaren_step.
  *   m [n], u [n,d], w [n]   float32, written.

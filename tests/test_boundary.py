@@ -112,3 +112,42 @@ def test_product_code_never_touches_the_oracle():
                 text = open(os.path.join(dirpath, fn)).read()
                 assert "import oracle" not in text and "from oracle" not in text, fn
                 assert "liboracle" not in text and "oracle.c" not in text, fn
+
+
+def test_reduce_workspace_and_argument_checks(lib):
+    # workspace: counters plus one state per part, parts bounded by the shape
+    assert binding.aaren_reduce_workspace_bytes(0, 4, 100, 64) == 0
+    assert binding.aaren_reduce_workspace_bytes(1, 1, 10, 17) == 2 ** 64 - 1
+    one = binding.aaren_reduce_workspace_bytes(1, 1, 1, 64)
+    assert one >= 256 + (64 + 4) * 4                       # N = 1: a single part
+    big = binding.aaren_reduce_workspace_bytes(1, 16, 1 << 20, 128)
+    assert (128 + 4) * 4 * 16 <= big <= 256 + 8192 * (128 + 4) * 4   # at most 8192 part states
+    fake = ctypes.c_void_p(256)
+    n = None
+    # unsupported d / dtype; negative size; nothing requested; partial state
+    assert lib.aaren_scan_reduce(fake, fake, fake, fake, 1, 1, 8, 48, 0, n, n, n, n, n, n, n, 0,
+                                 n) == binding.AAREN_ERR_UNSUPPORTED
+    assert lib.aaren_scan_reduce(fake, fake, fake, fake, 1, 1, 8, 64, 5, n, n, n, n, n, n, n, 0,
+                                 n) == binding.AAREN_ERR_UNSUPPORTED
+    assert lib.aaren_scan_reduce(fake, fake, fake, fake, 1, -1, 8, 64, 0, n, n, n, n, n, n, n, 0,
+                                 n) == binding.AAREN_ERR_INVALID
+    assert lib.aaren_scan_reduce(fake, fake, fake, n, 1, 1, 8, 64, 0, n, n, n, n, n, n, n, 0,
+                                 n) == binding.AAREN_ERR_INVALID
+    assert lib.aaren_scan_reduce(fake, fake, fake, fake, 1, 1, 8, 64, 0, n, n, n, fake, n, n, n, 0,
+                                 n) == binding.AAREN_ERR_INVALID
+    # the empty prefix has no output without a starting state
+    assert lib.aaren_scan_reduce(fake, n, n, fake, 1, 1, 0, 64, 0, n, n, n, n, n, n, n, 0,
+                                 n) == binding.AAREN_ERR_INVALID
+    # misaligned K; o_last overlapping V
+    assert lib.aaren_scan_reduce(fake, ctypes.c_void_p(260), fake, ctypes.c_void_p(1 << 20), 1, 1, 8,
+                                 64, 0, n, n, n, n, n, n, n, 0, n) == binding.AAREN_ERR_INVALID
+    assert lib.aaren_scan_reduce(fake, ctypes.c_void_p(1 << 20), ctypes.c_void_p(4096),
+                                 ctypes.c_void_p(4096 + 256), 1, 1, 8, 64, 0, n, n, n, n, n, n, n,
+                                 0, n) == binding.AAREN_ERR_INVALID
+    # a workspace that is too small is refused before anything runs
+    assert lib.aaren_scan_reduce(fake, fake, fake, ctypes.c_void_p(1 << 24), 1, 1, 8, 64, 0, n, n,
+                                 n, n, n, n, ctypes.c_void_p(1 << 25), 16,
+                                 n) == binding.AAREN_ERR_WORKSPACE
+    # no heads: nothing to do
+    assert lib.aaren_scan_reduce(n, n, n, fake, 0, 4, 8, 64, 0, n, n, n, n, n, n, n, 0,
+                                 n) == binding.AAREN_OK
