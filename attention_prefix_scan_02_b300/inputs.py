@@ -134,12 +134,15 @@ def default_threads() -> int:
         return os.cpu_count() or 1
 
 
-def batch_inputs(wl: Workload, device=None, threads: int | None = None):
+def batch_inputs(wl: Workload, device=None, threads: int | None = None, b0: int = 0):
     """All heads as torch tensors in the storage dtype:
     q [B, H, d], K [B, H, N, d], V [B, H, N, d].
 
-    Heads are drawn on a thread pool and copied into the (optionally device)
-    tensors one head at a time, so host memory holds only a few heads."""
+    Row b of the result holds batch entry b0 + b of the recipe (a shard of a
+    larger batch: with b0 = r * B, rank r of a multi-GPU run draws its own
+    heads).  Heads are drawn on a thread pool and copied into the (optionally
+    device) tensors one head at a time, so host memory holds only a few
+    heads."""
     import torch
     tdt = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
     dev = torch.device("cpu") if device is None else torch.device(device)
@@ -150,7 +153,7 @@ def batch_inputs(wl: Workload, device=None, threads: int | None = None):
 
     def one(bh):
         b, h = divmod(bh, wl.H)
-        qh, Kh, Vh = head_inputs(wl, b, h)
+        qh, Kh, Vh = head_inputs(wl, b0 + b, h)
         return bh, qh, Kh, Vh
 
     workers = min(threads, max(1, wl.heads))

@@ -313,7 +313,9 @@ def run_ours(args):
                          f"{passes} passes, {dt:.1f} s wall on {threads} threads "
                          f"(about {dt * threads:.0f} CPU-seconds)"}
 
-    q, K, V = inputs.batch_inputs(wl, device="cuda")
+    # rank r draws batch entries [r B, (r + 1) B) of the recipe: the ranks
+    # together process a batch of world * B sequences (weak scaling)
+    q, K, V = inputs.batch_inputs(wl, device="cuda", b0=rank * wl.B)
     reduce = args.op == "reduce"
     O = torch.empty((wl.B, wl.H, wl.d) if reduce else K.shape, dtype=out_t, device="cuda")
     ws = (binding.new_reduce_workspace if reduce else binding.new_workspace)(wl.B, wl.H, wl.N, wl.d)
@@ -432,7 +434,8 @@ def run_ours(args):
         "n_gpus": world, "steps": args.steps, "warmup": warmup, "ms_per_step": step_ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32", "data": "synthetic",
-        "config": dict(describe(wl, out), op=args.op),
+        "config": dict(describe(wl, out), op=args.op, global_batch=world * wl.B,
+                       parallelism=f"independent sequences, {world} rank(s), no collective"),
         "gpu_launches": args.steps,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,

@@ -67,3 +67,14 @@ def test_named_workloads():
     assert (w["stress"].B, w["stress"].H, w["stress"].N, w["stress"].d) == (4, 8, 16384, 64)
     assert (w["long"].B, w["long"].H, w["long"].N, w["long"].d, w["long"].dtype) == (1, 16, 1 << 20, 128, "bf16")
     assert (w["stream"].B, w["stream"].H, w["stream"].N, w["stream"].d) == (256, 8, 4096, 64)
+
+
+def test_batch_offset_draws_a_shard_of_a_larger_batch():
+    """Rank r of a multi-GPU run draws batch entries [r B, (r + 1) B): the
+    shards of all ranks together are the batch of world * B sequences."""
+    small = inputs.custom(1, 2, 40, 16, seed=21)
+    big = inputs.custom(3, 2, 40, 16, seed=21)
+    qb, Kb, Vb = inputs.batch_inputs(big)
+    for r in range(3):
+        q, K, V = inputs.batch_inputs(small, b0=r)
+        assert torch.equal(q[0], qb[r]) and torch.equal(K[0], Kb[r]) and torch.equal(V[0], Vb[r])
