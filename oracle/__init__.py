@@ -47,6 +47,16 @@ def _bind(path):
     lib.oracle_scan_longdouble.argtypes = [_f32p, _f32p, _f32p, _i64, _i64,
                                            _f64p, _f64p, _f64p, _f64p]
     lib.oracle_scan_longdouble.restype = ctypes.c_int
+    lib.oracle_lse_direct.argtypes = [_f64p, _i64, _f64p]
+    lib.oracle_lse_direct.restype = None
+    lib.oracle_lse.argtypes = [_f32p, _f32p, _i64, _i64, _f64p]
+    lib.oracle_lse.restype = ctypes.c_int
+    lib.oracle_backward_bruteforce.argtypes = [_f32p, _f32p, _f32p, _f32p, _i64, _i64,
+                                               _f64p, _f64p, _f64p, _f64p]
+    lib.oracle_backward_bruteforce.restype = None
+    lib.oracle_backward.argtypes = [_f32p, _f32p, _f32p, _f32p, _i64, _i64,
+                                    _f64p, _f64p, _f64p, _f64p]
+    lib.oracle_backward.restype = ctypes.c_int
     return lib
 
 
@@ -172,6 +182,65 @@ def scan_longdouble(q, K, V):
                                       _p64(m), _p64(u), _p64(w)) != 0:
         raise MemoryError("oracle_scan_longdouble: allocation failed")
     return O, float(m[0]), u, float(w[0])
+
+
+def lse_direct(s):
+    """log sum_{i<=t} e^{s_i} of every prefix t, each prefix summed afresh."""
+    s = _f64(s)
+    out = np.empty(len(s), dtype=np.float64)
+    _load().oracle_lse_direct(_p64(s), len(s), _p64(out))
+    return out
+
+
+def lse(q, K):
+    """log sum_{i<=t} e^{q.k_i} of every prefix t, in the running form."""
+    q, K = _f32(q), _f32(K)
+    N, d = K.shape
+    out = np.empty(N, dtype=np.float64)
+    if _load().oracle_lse(_p32(q), _p32(K), N, d, _p64(out)) != 0:
+        raise MemoryError("oracle_lse: allocation failed")
+    return out
+
+
+def backward_bruteforce(q, K, V, G):
+    """Gradients of L = sum_t G_t . o_t from their definition, O(N^2 d).
+    Returns (dq [d], dK [N,d], dV [N,d], ds [N]) in float64."""
+    q, K, V, G = _f32(q), _f32(K), _f32(V), _f32(G)
+    N, d = K.shape
+    dq = np.empty(d); dK = np.empty((N, d)); dV = np.empty((N, d)); ds = np.empty(N)
+    _load().oracle_backward_bruteforce(_p32(q), _p32(K), _p32(V), _p32(G), N, d, _p64(dq),
+                                       _p64(dK), _p64(dV), _p64(ds))
+    return dq, dK, dV, ds
+
+
+def backward(q, K, V, G):
+    """The same gradients by backward suffix sums, O(N d).
+    Returns (dq [d], dK [N,d], dV [N,d], ds [N]) in float64."""
+    q, K, V, G = _f32(q), _f32(K), _f32(V), _f32(G)
+    N, d = K.shape
+    dq = np.empty(d); dK = np.empty((N, d)); dV = np.empty((N, d)); ds = np.empty(N)
+    if _load().oracle_backward(_p32(q), _p32(K), _p32(V), _p32(G), N, d, _p64(dq), _p64(dK),
+                               _p64(dV), _p64(ds)) != 0:
+        raise MemoryError("oracle_backward: allocation failed")
+    return dq, dK, dV, ds
+
+
+def backward_heads(q, K, V, G, threads=1):
+    """backward() for independent heads: q [BH,d], K/V/G [BH,N,d]."""
+    q, K, V, G = _f32(q), _f32(K), _f32(V), _f32(G)
+    BH, N, d = K.shape
+    dq = np.empty((BH, d)); dK = np.empty((BH, N, d)); dV = np.empty((BH, N, d))
+
+    def one(h):
+        dq[h], dK[h], dV[h], _ = backward(q[h], K[h], V[h], G[h])
+
+    if threads <= 1:
+        for h in range(BH):
+            one(h)
+    else:
+        with ThreadPoolExecutor(max_workers=threads) as ex:
+            list(ex.map(one, range(BH)))
+    return dq, dK, dV
 
 
 def scan_heads(q, K, V, threads=1, want_O=True):

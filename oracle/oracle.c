@@ -250,3 +250,177 @@ int oracle_scan_longdouble(const float *q, const float *K, const float *V,
     free(u);
     return 0;
 }
+
+/* ======================================================================== */
+/* Differentiation of the many-to-many output.                              */
+/*                                                                          */
+/* The memory-efficient-attention review reports its method for inference   */
+/* and for differentiation (its abstract and section 5.2, whose body the    */
+/* page lacks); the Aaren review calls the RNN form exact and               */
+/* differentiable ("Proposed method").  For one head and an upstream        */
+/* gradient g_t = dL/do_t (t = 1..N), with p_{t,i} = e^{s_i} / sum_{j<=t}   */
+/* e^{s_j} for i <= t (so o_t = sum_{i<=t} p_{t,i} v_i):                     */
+/*                                                                          */
+/*   dL/dv_i = sum_{t>=i} p_{t,i} g_t                                       */
+/*   dL/ds_i = sum_{t>=i} p_{t,i} (g_t . v_i - g_t . o_t)                   */
+/*   dL/dq   = sum_i dL/ds_i k_i ,   dL/dk_i = dL/ds_i q                    */
+/*                                                                          */
+/* (the softmax Jacobian dp_{t,i}/ds_j = p_{t,i} (1[i=j] - p_{t,j})).       */
+/* ======================================================================== */
+
+/* Log of the softmax denominator of every prefix:                          */
+/*   lse_t = log sum_{i<=t} e^{s_i}, evaluated as max + log(sum e^{s-max})  */
+/* over the whole prefix (no running form).  O(N^2); used by the pins.      */
+void oracle_lse_direct(const double *s, int64_t N, double *lse)
+{
+    for (int64_t t = 0; t < N; ++t) {
+        double top = s[0];
+        for (int64_t i = 1; i <= t; ++i) top = (s[i] > top) ? s[i] : top;
+        double acc = 0.0;
+        for (int64_t i = 0; i <= t; ++i) acc += exp(s[i] - top);
+        lse[t] = top + log(acc);
+    }
+}
+
+/* The definition above written out: O(N^2 d), small N only.  ds may be    */
+/* NULL.  dq [d], dK [N,d], dV [N,d], ds [N] are written.                    */
+void oracle_backward_bruteforce(const float *q, const float *K, const float *V,
+                                const float *G, int64_t N, int64_t d,
+                                double *dq, double *dK, double *dV, double *ds)
+{
+    double *s = (double *)malloc((size_t)(N > 0 ? N : 1) * sizeof(double));
+    double *p = (double *)malloc((size_t)(N > 0 ? N : 1) * sizeof(double));
+    double *o = (double *)malloc((size_t)(d > 0 ? d : 1) * sizeof(double));
+    double *dsl = (double *)calloc((size_t)(N > 0 ? N : 1), sizeof(double));
+    for (int64_t i = 0; i < N; ++i) {
+        double acc = 0.0;
+        for (int64_t j = 0; j < d; ++j) acc += (double)q[j] * (double)K[i * d + j];
+        s[i] = acc;
+    }
+    for (int64_t x = 0; x < N * d; ++x) dV[x] = 0.0;
+    for (int64_t t = 0; t < N; ++t) {
+        /* softmax weights of prefix t and its output o_t */
+        double top = s[0];
+        for (int64_t i = 1; i <= t; ++i) top = (s[i] > top) ? s[i] : top;
+        double z = 0.0;
+        for (int64_t i = 0; i <= t; ++i) z += exp(s[i] - top);
+        for (int64_t i = 0; i <= t; ++i) p[i] = exp(s[i] - top) / z;
+        for (int64_t j = 0; j < d; ++j) {
+            double acc = 0.0;
+            for (int64_t i = 0; i <= t; ++i) acc += p[i] * (double)V[i * d + j];
+            o[j] = acc;
+        }
+        double go = 0.0;
+        for (int64_t j = 0; j < d; ++j) go += (double)G[t * d + j] * o[j];
+        for (int64_t i = 0; i <= t; ++i) {
+            double gv = 0.0;
+            for (int64_t j = 0; j < d; ++j) {
+                dV[i * d + j] += p[i] * (double)G[t * d + j];
+                gv += (double)G[t * d + j] * (double)V[i * d + j];
+            }
+            dsl[i] += p[i] * (gv - go);
+        }
+    }
+    for (int64_t j = 0; j < d; ++j) dq[j] = 0.0;
+    for (int64_t i = 0; i < N; ++i)
+        for (int64_t j = 0; j < d; ++j) {
+            dq[j] += dsl[i] * (double)K[i * d + j];
+            dK[i * d + j] = dsl[i] * (double)q[j];
+        }
+    if (ds)
+        for (int64_t i = 0; i < N; ++i) ds[i] = dsl[i];
+    free(s);
+    free(p);
+    free(o);
+    free(dsl);
+}
+
+/* The same gradients in O(N d): the sums over t >= i run backwards, token  */
+/* by token, as the two suffix sums                                         */
+/*   R_i = sum_{t>=i} e^{lse_i - lse_t} g_t,                                */
+/*   D_i = sum_{t>=i} e^{lse_i - lse_t} (g_t . o_t)                         */
+/* (every weight <= 1, as lse never decreases along the sequence), so that  */
+/*   R_i = g_i + e^{lse_i - lse_{i+1}} R_{i+1}   (same for D),              */
+/*   dL/dv_i = e^{s_i - lse_i} R_i,                                         */
+/*   dL/ds_i = e^{s_i - lse_i} (v_i . R_i - D_i).                           */
+/* lse_t and o_t come from a forward pass in the running form (the          */
+/* recurrence of oracle_scan_scores, with lse_t = m_t + log w_t).           */
+/* ds may be NULL.  Returns nonzero when scratch allocation fails.          */
+int oracle_backward(const float *q, const float *K, const float *V,
+                    const float *G, int64_t N, int64_t d, double *dq,
+                    double *dK, double *dV, double *ds)
+{
+    double *s = (double *)malloc((size_t)(N > 0 ? N : 1) * sizeof(double));
+    double *lse = (double *)malloc((size_t)(N > 0 ? N : 1) * sizeof(double));
+    double *O = (double *)malloc((size_t)(N > 0 ? N : 1) * (d > 0 ? d : 1) * sizeof(double));
+    double *R = (double *)calloc((size_t)(d > 0 ? d : 1), sizeof(double));
+    if (!s || !lse || !O || !R) {
+        free(s);
+        free(lse);
+        free(O);
+        free(R);
+        return 1;
+    }
+    oracle_scores(q, K, N, d, s);
+    /* forward: running maximum and rescaled sum give lse_t; outputs o_t */
+    {
+        double run_max = -INFINITY, run_sum = 0.0;
+        for (int64_t t = 0; t < N; ++t) {
+            double hi = (s[t] > run_max) ? s[t] : run_max;
+            run_sum = run_sum * ((run_max == -INFINITY) ? 0.0 : exp(run_max - hi)) + exp(s[t] - hi);
+            run_max = hi;
+            lse[t] = run_max + log(run_sum);
+        }
+        oracle_scan_scores(s, V, N, d, NULL, NULL, NULL, O, NULL, NULL, NULL);
+    }
+    /* backward: suffix sums from the last token down */
+    double D = 0.0;
+    for (int64_t j = 0; j < d; ++j) dq[j] = 0.0;
+    for (int64_t i = N - 1; i >= 0; --i) {
+        if (i + 1 < N) {
+            double decay = exp(lse[i] - lse[i + 1]);
+            for (int64_t j = 0; j < d; ++j) R[j] *= decay;
+            D *= decay;
+        }
+        double go = 0.0, vr = 0.0;
+        for (int64_t j = 0; j < d; ++j) {
+            go += (double)G[i * d + j] * O[i * d + j];
+            R[j] += (double)G[i * d + j];
+        }
+        D += go;
+        double pii = exp(s[i] - lse[i]);
+        for (int64_t j = 0; j < d; ++j) {
+            dV[i * d + j] = pii * R[j];
+            vr += (double)V[i * d + j] * R[j];
+        }
+        double dsi = pii * (vr - D);
+        for (int64_t j = 0; j < d; ++j) {
+            dK[i * d + j] = dsi * (double)q[j];
+            dq[j] += dsi * (double)K[i * d + j];
+        }
+        if (ds) ds[i] = dsi;
+    }
+    free(s);
+    free(lse);
+    free(O);
+    free(R);
+    return 0;
+}
+
+/* lse_t of every prefix in the running form (as oracle_backward's forward  */
+/* pass); the value the library's forward writes next to O for a backward.  */
+int oracle_lse(const float *q, const float *K, int64_t N, int64_t d, double *lse)
+{
+    double *s = (double *)malloc((size_t)(N > 0 ? N : 1) * sizeof(double));
+    if (!s) return 1;
+    oracle_scores(q, K, N, d, s);
+    double run_max = -INFINITY, run_sum = 0.0;
+    for (int64_t t = 0; t < N; ++t) {
+        double hi = (s[t] > run_max) ? s[t] : run_max;
+        run_sum = run_sum * ((run_max == -INFINITY) ? 0.0 : exp(run_max - hi)) + exp(s[t] - hi);
+        run_max = hi;
+        lse[t] = run_max + log(run_sum);
+    }
+    free(s);
+    return 0;
+}

@@ -26,6 +26,17 @@ What pins what:
   continuation     scanning [A; B] equals scanning B from A's final state
   running sum      the unscaled running sums of the memory-efficient-attention
                    review (section 2) agree when the scores are moderate
+Differentiation (gradients of L = sum_t g_t . o_t):
+  finite diff.     central differences of L computed by an independent numpy
+                   forward (per-prefix scipy.special.softmax, matmuls)
+  suffix sums      the O(N d) backward equals the O(N^2 d) definition
+  shift            sum_i dL/ds_i = 0 (L does not change when every score
+                   moves by the same constant)
+  one token        o_1 = v_1, so dL/dv_1 = g_1 and every score gradient is 0
+  equal scores     q = 0: dL/dv_i = sum_{t>=i} g_t / t
+  log-sum-exp      lse_t (running form) equals scipy.special.logsumexp of
+                   every prefix and the per-prefix direct form
+  large scores     |s| in the hundreds: the backward stays finite and agrees
 """
 import os
 from fractions import Fraction
@@ -278,9 +289,106 @@ def pin_running_sum():
     assert _rel(O, ref) < 1e-12
 
 
+def _numpy_loss(q, K, V, G):
+    """L = sum_t G_t . o_t with o_t the per-prefix softmax of q.k_i over V,
+    in numpy float64 (independent of the oracle's C code)."""
+    s = K @ q
+    total = 0.0
+    for t in range(len(s)):
+        p = scipy.special.softmax(s[:t + 1])
+        total += float(G[t] @ (p @ V[:t + 1]))
+    return total
+
+
+def _small(seed, N, d, scale=1.0):
+    r = _rng(seed)
+    f = lambda *shape: r.standard_normal(shape).astype(np.float32)
+    return f(d) * np.float32(scale), f(N, d), f(N, d), f(N, d)
+
+
+def pin_backward_finite_differences():
+    for seed, N, d in ((1, 6, 3), (2, 11, 4), (3, 1, 2)):
+        q, K, V, G = _small(seed, N, d)
+        dq, dK, dV, _ = oracle.backward_bruteforce(q, K, V, G)
+        q64, K64, V64, G64 = (x.astype(np.float64) for x in (q, K, V, G))
+        h = 1e-5
+        r = _rng(100 + seed)
+        checks = [("q", j, None) for j in range(d)]
+        checks += [("K", int(r.integers(N)), int(r.integers(d))) for _ in range(4)]
+        checks += [("V", int(r.integers(N)), int(r.integers(d))) for _ in range(4)]
+        for name, a, b in checks:
+            base = {"q": q64, "K": K64, "V": V64}[name]
+            plus, minus = base.copy(), base.copy()
+            idx = (a,) if b is None else (a, b)
+            plus[idx] += h
+            minus[idx] -= h
+            args_p = {"q": q64, "K": K64, "V": V64, name: plus}
+            args_m = {"q": q64, "K": K64, "V": V64, name: minus}
+            fd = (_numpy_loss(args_p["q"], args_p["K"], args_p["V"], G64) -
+                  _numpy_loss(args_m["q"], args_m["K"], args_m["V"], G64)) / (2 * h)
+            an = {"q": dq, "K": dK, "V": dV}[name][idx]
+            assert abs(fd - an) <= 1e-6 * max(1.0, abs(fd)), (name, idx, fd, an)
+
+
+def pin_backward_suffix_sums():
+    for seed, N, d in ((4, 1, 1), (5, 2, 3), (6, 17, 5), (7, 40, 8)):
+        q, K, V, G = _small(seed, N, d, scale=2.0)
+        ref = oracle.backward_bruteforce(q, K, V, G)
+        got = oracle.backward(q, K, V, G)
+        # dL/ds_i is a difference of two sums that nearly cancel: a few
+        # hundred ulps of float64 apart at most when both are right
+        for a, b in zip(got, ref):
+            assert _rel(a, b) < 1e-10
+
+
+def pin_backward_shift():
+    q, K, V, G = _small(8, 30, 6, scale=3.0)
+    _, _, _, ds = oracle.backward(q, K, V, G)
+    assert abs(float(np.sum(ds))) <= 1e-12 * float(np.sum(np.abs(ds)))
+
+
+def pin_backward_one_token():
+    q, K, V, G = _small(9, 1, 5)
+    dq, dK, dV, ds = oracle.backward(q, K, V, G)
+    assert np.array_equal(dV[0], G[0].astype(np.float64))
+    assert abs(ds[0]) <= 1e-15 and np.max(np.abs(dq)) <= 1e-15 and np.max(np.abs(dK)) <= 1e-15
+
+
+def pin_backward_equal_scores():
+    _, K, V, G = _small(10, 25, 4)
+    q = np.zeros(4, dtype=np.float32)
+    _, _, dV, _ = oracle.backward(q, K, V, G)
+    t = np.arange(1, 26, dtype=np.float64)[:, None]
+    ref = np.cumsum((G.astype(np.float64) / t)[::-1], axis=0)[::-1]
+    assert _rel(dV, ref) < 1e-13
+
+
+def pin_lse():
+    q, K, _, _ = _small(11, 50, 6, scale=4.0)
+    got = oracle.lse(q, K)
+    s = oracle.scores(q, K)
+    ref = np.array([scipy.special.logsumexp(s[:t + 1]) for t in range(len(s))])
+    assert _rel(got, ref) < 1e-13
+    assert _rel(oracle.lse_direct(s), ref) < 1e-13
+
+
+def pin_backward_large_scores():
+    q, K, V, G = _small(12, 60, 4)
+    K = (K * np.float32(60.0)).astype(np.float32)    # scores of several hundred
+    s = oracle.scores(q, K)
+    assert np.max(np.abs(s)) > 150
+    got = oracle.backward(q, K, V, G)
+    ref = oracle.backward_bruteforce(q, K, V, G)
+    for a, b in zip(got, ref):
+        assert np.all(np.isfinite(a))
+        assert _rel(a, b) < 1e-11
+
+
 ALL_PINS = [
     pin_worked_example, pin_bruteforce, pin_last_row, pin_scores, pin_shift,
     pin_equal_scores, pin_hillis_steele, pin_operator_laws, pin_first_output,
     pin_one_hot, pin_bounds, pin_long_double, pin_large_scores, pin_continuation,
-    pin_running_sum,
+    pin_running_sum, pin_backward_finite_differences, pin_backward_suffix_sums,
+    pin_backward_shift, pin_backward_one_token, pin_backward_equal_scores, pin_lse,
+    pin_backward_large_scores,
 ]

@@ -45,6 +45,17 @@ MUTANTS = {
                 "        for (int64_t j = 0; j < d; ++j) u_out[j] = u[j];\n    free(u);\n}\n\n"
                 "/* Scores"),
     "longdouble_sign": ("long double b = expl(s - M);", "long double b = expl(M - s);"),
+    # differentiation
+    "bwd_decay_sign": ("double decay = exp(lse[i] - lse[i + 1]);",
+                       "double decay = exp(lse[i + 1] - lse[i]);"),
+    "bwd_dropped_D": ("double dsi = pii * (vr - D);", "double dsi = pii * vr;"),
+    "bwd_brute_dropped_go": ("dsl[i] += p[i] * (gv - go);", "dsl[i] += p[i] * gv;"),
+    "bwd_brute_grad_index": ("dV[i * d + j] += p[i] * (double)G[t * d + j];",
+                             "dV[i * d + j] += p[i] * (double)G[i * d + j];"),
+    "bwd_dk_transposed": ("dK[i * d + j] = dsi * (double)q[j];",
+                          "dK[i * d + j] = dsi * (double)K[i * d + j];"),
+    "lse_direct_exclusive": ("for (int64_t i = 0; i <= t; ++i) acc += exp(s[i] - top);",
+                             "for (int64_t i = 0; i < t; ++i) acc += exp(s[i] - top);"),
 }
 
 
