@@ -35,6 +35,7 @@ EXPORTS = (
     "aaren_state_init", "aaren_step", "aaren_check", "aaren_status_string",
     "aaren_abi_version", "aaren_debug_set_fault", "aaren_scan_chunk_tokens",
     "aaren_scan_forward_noalloc", "aaren_scan_reduce", "aaren_reduce_workspace_bytes",
+    "aaren_scan_forward_stats", "aaren_scan_backward", "aaren_backward_workspace_bytes",
 )
 
 # size of the fixed device scratch of aaren_scan_forward_noalloc (include/aaren.h)
@@ -92,6 +93,14 @@ def load(path: str | None = None):
     lib.aaren_scan_reduce.restype = _i32
     lib.aaren_reduce_workspace_bytes.argtypes = [_i64, _i64, _i64, _i64]
     lib.aaren_reduce_workspace_bytes.restype = ctypes.c_size_t
+    lib.aaren_scan_forward_stats.argtypes = [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i32,
+                                             _vp, ctypes.c_size_t, _vp]
+    lib.aaren_scan_forward_stats.restype = _i32
+    lib.aaren_scan_backward.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64,
+                                        _i64, _i64, _i32, _vp, ctypes.c_size_t, _vp]
+    lib.aaren_scan_backward.restype = _i32
+    lib.aaren_backward_workspace_bytes.argtypes = [_i64, _i64, _i64, _i64]
+    lib.aaren_backward_workspace_bytes.restype = ctypes.c_size_t
     if path is None:
         _lib = lib
     return lib
@@ -243,6 +252,54 @@ def aaren_scan_reduce(q, K, V, o_last=None, m_in=None, u_in=None, w_in=None, m_o
     return o_last
 
 
+def aaren_backward_workspace_bytes(B: int, H: int, N: int, d: int) -> int:
+    return int(load().aaren_backward_workspace_bytes(B, H, N, d))
+
+
+def aaren_scan_forward_stats(q, K, V, O, stats, workspace=None, stream=None):
+    """aaren_scan_forward that also writes stats [B,H,N,2] float32: the
+    (m_t, w_t) of every prefix, which aaren_scan_backward needs."""
+    lib = load()
+    B, H, N, d = K.shape
+    if tuple(V.shape) != (B, H, N, d) or tuple(O.shape) != (B, H, N, d) or tuple(q.shape) != (B, H, d):
+        raise ValueError("q [B,H,d], K/V/O [B,H,N,d]")
+    if stats.dtype != torch.float32 or stats.numel() != B * H * N * 2:
+        raise ValueError("stats must be float32 [B, H, N, 2]")
+    _check_cuda(q, K, V, O, stats, workspace)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = lib.aaren_scan_forward_stats(_ptr(q), _ptr(K), _ptr(V), _ptr(O), _ptr(stats), B, H, N, d,
+                                      dtype_code(K.dtype, O.dtype), _ptr(workspace), ws_bytes,
+                                      _stream_handle(stream))
+    _raise(rc, "aaren_scan_forward_stats")
+    return O, stats
+
+
+def aaren_scan_backward(q, K, V, O, dO, stats, dq, dK, dV, workspace=None, stream=None):
+    """Gradients dq [B*H,d], dK, dV [B,H,N,d] (float32, written) of the
+    many-to-many output, given its upstream gradient dO and the forward's
+    O and stats."""
+    lib = load()
+    B, H, N, d = K.shape
+    for t in (V, O, dO, dK, dV):
+        if tuple(t.shape) != (B, H, N, d):
+            raise ValueError("K, V, O, dO, dK, dV must be [B, H, N, d]")
+    if tuple(q.shape) != (B, H, d) or dq.numel() != B * H * d:
+        raise ValueError("q must be [B, H, d] and dq hold [B*H, d]")
+    if O.dtype != dO.dtype:
+        raise ValueError("O and dO share the output dtype")
+    for t in (dq, dK, dV, stats):
+        if t.dtype != torch.float32:
+            raise ValueError("gradients and stats are float32")
+    _check_cuda(q, K, V, O, dO, stats, dq, dK, dV, workspace)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = lib.aaren_scan_backward(_ptr(q), _ptr(K), _ptr(V), _ptr(O), _ptr(dO), _ptr(stats),
+                                 _ptr(dq), _ptr(dK), _ptr(dV), B, H, N, d,
+                                 dtype_code(K.dtype, O.dtype), _ptr(workspace), ws_bytes,
+                                 _stream_handle(stream))
+    _raise(rc, "aaren_scan_backward")
+    return dq, dK, dV
+
+
 def aaren_state_init(m, u, w, stream=None):
     """Identity state (-inf, 0, 0): m [n], u [n, d], w [n] (float32)."""
     n, d = u.shape
@@ -324,6 +381,30 @@ def scan_reduce(q, K, V, out_dtype=None, init=None, return_state=False, workspac
 
 def new_reduce_workspace(B, H, N, d, device="cuda"):
     nbytes = aaren_reduce_workspace_bytes(B, H, N, d)
+    return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+
+
+def scan_forward_train(q, K, V, out_dtype=None, stream=None):
+    """Forward for a later backward: returns (O, stats)."""
+    out_dtype = out_dtype or K.dtype
+    B, H, N, d = K.shape
+    O = torch.empty(K.shape, dtype=out_dtype, device=K.device)
+    stats = torch.empty(B, H, N, 2, dtype=torch.float32, device=K.device)
+    return aaren_scan_forward_stats(q, K, V, O, stats, stream=stream)
+
+
+def scan_backward(q, K, V, O, dO, stats, workspace=None, stream=None):
+    """Allocate and return (dq [B,H,d], dK, dV [B,H,N,d]) in float32."""
+    B, H, N, d = K.shape
+    dq = torch.empty(B, H, d, dtype=torch.float32, device=K.device)
+    dK = torch.empty(K.shape, dtype=torch.float32, device=K.device)
+    dV = torch.empty(K.shape, dtype=torch.float32, device=K.device)
+    aaren_scan_backward(q, K, V, O, dO, stats, dq, dK, dV, workspace, stream)
+    return dq, dK, dV
+
+
+def new_backward_workspace(B, H, N, d, device="cuda"):
+    nbytes = aaren_backward_workspace_bytes(B, H, N, d)
     return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
 
 

@@ -14,6 +14,7 @@
 #include "scan_kernel.cuh"
 #include "scan_pipe_kernel.cuh"
 #include "reduce_kernel.cuh"
+#include "bwd_kernel.cuh"
 #include "step_kernel.cuh"
 
 namespace aaren {
@@ -243,6 +244,85 @@ aaren_status_t check_state(const float *m, const float *u, const float *w)
     return AAREN_OK;
 }
 
+// ---------------------------------------------------------------- backward
+
+int64_t bwd_chunk_tokens(int64_t d, int32_t dtype)
+{
+    switch (d) {
+#define AAREN_BWD_C(DD)                                                                          \
+    case DD:                                                                                     \
+        return dtype == AAREN_F32 ? BwdTile<DD, float, float>::C                                 \
+               : dtype == AAREN_BF16 ? BwdTile<DD, __nv_bfloat16, __nv_bfloat16>::C              \
+                                     : BwdTile<DD, __nv_bfloat16, float>::C;
+        AAREN_BWD_C(16)
+        AAREN_BWD_C(32)
+        AAREN_BWD_C(64)
+        AAREN_BWD_C(128)
+#undef AAREN_BWD_C
+    default: return 0;
+    }
+}
+
+struct BwdLayout {
+    size_t flags_off, states_off, acc_off, count_off, bytes, zero_from, zero_bytes;
+    int64_t chunks_per_head, total_chunks;
+};
+
+// [ticket | pad 256] [flags] [states: 2 per chunk] [dq accumulator: heads x d
+// floats] [dq counters: heads]; the ticket, flags, accumulator and counters
+// are zeroed before a launch (two ranges).
+bool bwd_layout(int64_t BH, int64_t N, int64_t d, int64_t C, BwdLayout *w)
+{
+    if (C <= 0) return false;
+    const int64_t cph = (N + C - 1) / C;
+    int64_t total;
+    if (!mul_ok(BH, cph, &total) || total > INT_MAX) return false;
+    w->chunks_per_head = cph;
+    w->total_chunks = total;
+    const size_t flag_bytes = ((size_t(total) * 4 + 255) / 256) * 256;
+    w->flags_off = kHeaderBytes;
+    w->states_off = kHeaderBytes + flag_bytes;
+    w->acc_off = w->states_off + size_t(total) * 2 * size_t(d + 4) * sizeof(float);
+    w->count_off = w->acc_off + ((size_t(BH) * d * 4 + 255) / 256) * 256;
+    w->bytes = w->count_off + ((size_t(BH) * 4 + 255) / 256) * 256;
+    w->zero_from = w->acc_off;
+    w->zero_bytes = kHeaderBytes + flag_bytes;   // first range; the second is [acc_off, bytes)
+    return true;
+}
+
+template <int D, typename Tin, typename Tout>
+aaren_status_t launch_bwd(const BwdParams &p, int64_t total, cudaStream_t st)
+{
+    using Tile = BwdTile<D, Tin, Tout>;
+    static std::atomic<unsigned long long> configured{0};
+    auto kern = k_scan_bwd<D, Tin, Tout>;
+    if (allow_smem(kern, Tile::smem_bytes, configured) != cudaSuccess) return AAREN_ERR_CUDA;
+    kern<<<unsigned(total), Tile::WARPS * 32, Tile::smem_bytes, st>>>(p);
+    return cudaGetLastError() == cudaSuccess ? AAREN_OK : AAREN_ERR_CUDA;
+}
+
+template <int D>
+aaren_status_t dispatch_bwd_dtype(const BwdParams &p, int64_t total, int32_t dtype, cudaStream_t st)
+{
+    switch (dtype) {
+    case AAREN_F32: return launch_bwd<D, float, float>(p, total, st);
+    case AAREN_BF16: return launch_bwd<D, __nv_bfloat16, __nv_bfloat16>(p, total, st);
+    case AAREN_BF16_F32OUT: return launch_bwd<D, __nv_bfloat16, float>(p, total, st);
+    default: return AAREN_ERR_UNSUPPORTED;
+    }
+}
+
+aaren_status_t dispatch_bwd(const BwdParams &p, int64_t total, int64_t d, int32_t dtype, cudaStream_t st)
+{
+    switch (d) {
+    case 16: return dispatch_bwd_dtype<16>(p, total, dtype, st);
+    case 32: return dispatch_bwd_dtype<32>(p, total, dtype, st);
+    case 64: return dispatch_bwd_dtype<64>(p, total, dtype, st);
+    case 128: return dispatch_bwd_dtype<128>(p, total, dtype, st);
+    default: return AAREN_ERR_UNSUPPORTED;
+    }
+}
+
 // ---------------------------------------------------------------- reduce
 
 // Parts per head the workspace is sized for: at most 8192 part states in
@@ -347,11 +427,11 @@ size_t aaren_scan_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t d)
     return w.bytes;
 }
 
-aaren_status_t aaren_scan_forward_ex(const void *q, const void *K, const void *V, void *O,
-                                     int64_t B, int64_t H, int64_t N, int64_t d, int32_t dtype,
-                                     const float *m_in, const float *u_in, const float *w_in,
-                                     float *m_out, float *u_out, float *w_out, void *workspace,
-                                     size_t workspace_bytes, void *stream)
+static aaren_status_t scan_forward_impl(const void *q, const void *K, const void *V, void *O,
+                                        int64_t B, int64_t H, int64_t N, int64_t d, int32_t dtype,
+                                        const float *m_in, const float *u_in, const float *w_in,
+                                        float *m_out, float *u_out, float *w_out, float *stats,
+                                        void *workspace, size_t workspace_bytes, void *stream)
 {
     if (!supported_dtype(dtype) || !supported_d(d)) return AAREN_ERR_UNSUPPORTED;
     if (B < 0 || H < 0 || N < 0) return AAREN_ERR_INVALID;
@@ -409,12 +489,101 @@ aaren_status_t aaren_scan_forward_ex(const void *q, const void *K, const void *V
             p.flags = reinterpret_cast<unsigned *>(base + wl.flags_off);
             p.states = reinterpret_cast<float *>(base + wl.states_off);
             p.status = status;
+            p.stats = reinterpret_cast<float2 *>(stats);
             p.N = N;
             p.heads = BH;
             p.chunks_per_head = wl.chunks_per_head;
             p.fault_chunk = g_fault_chunk.load();
             p.wait_limit_ns = g_wait_limit_ns.load();
             rc = dispatch_scan(p, wl.total_chunks, d, dtype, st);
+        }
+    }
+    if (owned && cudaFreeAsync(ws, st) != cudaSuccess && rc == AAREN_OK) rc = AAREN_ERR_CUDA;
+    return rc;
+}
+
+size_t aaren_backward_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t d)
+{
+    if (!supported_d(d) || B < 0 || H < 0 || N < 0) return SIZE_MAX;
+    int64_t BH;
+    if (!mul_ok(B, H, &BH)) return SIZE_MAX;
+    if (BH == 0 || N == 0) return 0;
+    int64_t C = bwd_chunk_tokens(d, AAREN_F32);   // the smallest chunk of any dtype
+    for (int32_t t : {AAREN_BF16, AAREN_BF16_F32OUT}) {
+        const int64_t c = bwd_chunk_tokens(d, t);
+        if (c < C) C = c;
+    }
+    BwdLayout w;
+    if (!bwd_layout(BH, N, d, C, &w)) return SIZE_MAX;
+    return w.bytes;
+}
+
+aaren_status_t aaren_scan_backward(const void *q, const void *K, const void *V, const void *O,
+                                   const void *dO, const float *stats, float *dq, float *dK, float *dV,
+                                   int64_t B, int64_t H, int64_t N, int64_t d, int32_t dtype,
+                                   void *workspace, size_t workspace_bytes, void *stream)
+{
+    if (!supported_dtype(dtype) || !supported_d(d)) return AAREN_ERR_UNSUPPORTED;
+    if (B < 0 || H < 0 || N < 0) return AAREN_ERR_INVALID;
+    int64_t BH, BHN, elems;
+    if (!mul_ok(B, H, &BH) || !mul_ok(BH, N, &BHN) || !mul_ok(BHN, d, &elems)) return AAREN_ERR_INVALID;
+    int64_t in_b, out_b, grad_b;
+    if (!mul_ok(elems, int64_t(in_elem_bytes(dtype)), &in_b) ||
+        !mul_ok(elems, int64_t(out_elem_bytes(dtype)), &out_b) || !mul_ok(elems, 4, &grad_b))
+        return AAREN_ERR_INVALID;
+    if (BH == 0) return AAREN_OK;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (dq == nullptr || !aligned(dq, 16)) return AAREN_ERR_INVALID;
+    if (N == 0)   // nothing depends on q: its gradient is zero
+        return cudaMemsetAsync(dq, 0, size_t(BH) * d * sizeof(float), st) == cudaSuccess
+                   ? AAREN_OK : AAREN_ERR_CUDA;
+    const void *ins[] = {q, K, V, O, dO, stats, dK, dV};
+    for (const void *x : ins)
+        if (x == nullptr || !aligned(x, 16)) return AAREN_ERR_INVALID;
+    // the gradients must not overlap any input
+    const void *rd[] = {K, V, O, dO};
+    const size_t rd_b[] = {size_t(in_b), size_t(in_b), size_t(out_b), size_t(out_b)};
+    for (int i = 0; i < 4; ++i)
+        if (overlaps(dK, size_t(grad_b), rd[i], rd_b[i]) || overlaps(dV, size_t(grad_b), rd[i], rd_b[i]))
+            return AAREN_ERR_INVALID;
+    if (overlaps(dK, size_t(grad_b), dV, size_t(grad_b))) return AAREN_ERR_INVALID;
+
+    const int64_t C = bwd_chunk_tokens(d, dtype);
+    BwdLayout wl;
+    if (!bwd_layout(BH, N, d, C, &wl)) return AAREN_ERR_INVALID;
+    void *ws = workspace;
+    bool owned = false;
+    if (ws == nullptr) {
+        if (cudaMallocAsync(&ws, wl.bytes, st) != cudaSuccess) return AAREN_ERR_CUDA;
+        owned = true;
+    } else if (workspace_bytes < wl.bytes || !aligned(ws, 256)) {
+        return AAREN_ERR_WORKSPACE;
+    }
+    aaren_status_t rc = AAREN_OK;
+    char *base = static_cast<char *>(ws);
+    if (cudaMemsetAsync(base, 0, wl.zero_bytes, st) != cudaSuccess ||
+        cudaMemsetAsync(base + wl.zero_from, 0, wl.bytes - wl.zero_from, st) != cudaSuccess) {
+        rc = AAREN_ERR_CUDA;
+    } else {
+        unsigned *status = nullptr;
+        if (cudaGetSymbolAddress(reinterpret_cast<void **>(&status), g_status) != cudaSuccess) {
+            rc = AAREN_ERR_CUDA;
+        } else {
+            BwdParams p;
+            p.q = q; p.K = K; p.V = V; p.O = O; p.dO = dO;
+            p.stats = reinterpret_cast<const float2 *>(stats);
+            p.dq = dq; p.dK = dK; p.dV = dV;
+            p.ticket = reinterpret_cast<unsigned *>(base);
+            p.flags = reinterpret_cast<unsigned *>(base + wl.flags_off);
+            p.states = reinterpret_cast<float *>(base + wl.states_off);
+            p.dq_acc = reinterpret_cast<float *>(base + wl.acc_off);
+            p.dq_count = reinterpret_cast<unsigned *>(base + wl.count_off);
+            p.status = status;
+            p.N = N;
+            p.heads = BH;
+            p.chunks_per_head = wl.chunks_per_head;
+            p.wait_limit_ns = g_wait_limit_ns.load();
+            rc = dispatch_bwd(p, wl.total_chunks, d, dtype, st);
         }
     }
     if (owned && cudaFreeAsync(ws, st) != cudaSuccess && rc == AAREN_OK) rc = AAREN_ERR_CUDA;
@@ -485,6 +654,27 @@ aaren_status_t aaren_scan_reduce(const void *q, const void *K, const void *V, vo
     }
     if (owned && cudaFreeAsync(ws, st) != cudaSuccess && rc == AAREN_OK) rc = AAREN_ERR_CUDA;
     return rc;
+}
+
+aaren_status_t aaren_scan_forward_ex(const void *q, const void *K, const void *V, void *O,
+                                     int64_t B, int64_t H, int64_t N, int64_t d, int32_t dtype,
+                                     const float *m_in, const float *u_in, const float *w_in,
+                                     float *m_out, float *u_out, float *w_out, void *workspace,
+                                     size_t workspace_bytes, void *stream)
+{
+    return scan_forward_impl(q, K, V, O, B, H, N, d, dtype, m_in, u_in, w_in, m_out, u_out, w_out,
+                             nullptr, workspace, workspace_bytes, stream);
+}
+
+aaren_status_t aaren_scan_forward_stats(const void *q, const void *K, const void *V, void *O,
+                                        float *stats, int64_t B, int64_t H, int64_t N, int64_t d,
+                                        int32_t dtype, void *workspace, size_t workspace_bytes,
+                                        void *stream)
+{
+    if (N > 0 && stats == nullptr) return AAREN_ERR_INVALID;
+    if (!aligned(stats, 8)) return AAREN_ERR_INVALID;
+    return scan_forward_impl(q, K, V, O, B, H, N, d, dtype, nullptr, nullptr, nullptr, nullptr,
+                             nullptr, nullptr, stats, workspace, workspace_bytes, stream);
 }
 
 aaren_status_t aaren_scan_forward(const void *q, const void *K, const void *V, void *O, int64_t B,

@@ -62,6 +62,7 @@ struct ScanParams {
     unsigned *ticket;    // workspace: ticket counter (zeroed before launch)
     unsigned *flags;     // workspace: one flag per chunk (zeroed before launch)
     float *states;       // workspace: per chunk [aggregate | inclusive] states
+    float2 *stats;       // optional [heads, N]: (m_t, w_t) of every prefix, for a backward pass
     unsigned *status;    // device status word
     int64_t N;
     int64_t heads;           // B * H
@@ -349,7 +350,8 @@ __device__ bool lookback(const ScanParams &p, int64_t head, int64_t c, float &xm
 template <int D, typename Tin, typename Tout, bool FULL>
 __device__ __forceinline__ void rescan_group(float sl, float &rm, float &rw,
                                              float (&u)[VLayout<D>::E], const Tin *vrow,
-                                             Tout *orow, float4 *cf, int ntok, int lane)
+                                             Tout *orow, float4 *cf, int ntok, int lane,
+                                             float2 *strow)
 {
     using L = VLayout<D>;
     constexpr int E = L::E;
@@ -378,6 +380,7 @@ __device__ __forceinline__ void rescan_group(float sl, float &rm, float &rw,
     }
     const float wt = fmaf(A, rw, Bc);
     const float rcp = (sl == -INFINITY) ? 0.f : __frcp_rn(wt);
+    if (strow != nullptr && lane < ntok) strow[lane] = make_float2(M, wt);   // this prefix's (m, w)
     cf[lane] = make_float4(alpha, beta, rcp, 0.f);
     __syncwarp();
     rm = __shfl_sync(kFull, M, 31);
@@ -605,10 +608,11 @@ __global__ void __launch_bounds__(WARPS * 32)
             const Tin *vrow = Vs + size_t(base) * D + lane * E;
             Tout *orow = static_cast<Tout *>(p.O) + size_t(row0 + base) * D + lane * E;
             if (base + 32 <= nvalid)
-                rescan_group<D, Tin, Tout, true>(s[g], rm, rw, u, vrow, orow, cf, 32, lane);
+                rescan_group<D, Tin, Tout, true>(s[g], rm, rw, u, vrow, orow, cf, 32, lane,
+                                                 p.stats ? p.stats + (row0 + base) : nullptr);
             else
                 rescan_group<D, Tin, Tout, false>(s[g], rm, rw, u, vrow, orow, cf, nvalid - base,
-                                                  lane);
+                                                  lane, p.stats ? p.stats + (row0 + base) : nullptr);
         }
     }
 }

@@ -596,6 +596,8 @@ __global__ void __launch_bounds__(PipeTile<D, GROUPS, STAGES>::THREADS, 1)
             }
             const float wt = fmaf(A, rw, Bc);
             const float rcp = (s == -INFINITY) ? 0.f : __frcp_rn(wt);
+            if (p.stats != nullptr && lane < nv)   // this prefix's (m, w), for a backward pass
+                p.stats[size_t(head * p.N + t0 + wg * 32) + lane] = make_float2(M, wt);
             cf[lane] = make_float4(alpha, beta, rcp, 0.f);   // .w: the zero for unpack_row_late
             __syncwarp();
             Tout *orow = static_cast<Tout *>(p.O) + size_t(head * p.N + t0 + wg * 32) * D + lane * E;

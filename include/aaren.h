@@ -120,6 +120,57 @@ aaren_status_t aaren_scan_forward_ex(const void *q, const void *K,
 size_t aaren_scan_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t d);
 
 /*
+ * aaren_scan_forward_stats -- aaren_scan_forward that also saves, for every
+ * prefix t, the pair (m_t, w_t) of its state: the running maximum of the
+ * scores and the rescaled sum of their exponentials, so that
+ * log sum_{i<=t} e^{s_i} = m_t + log w_t.  aaren_scan_backward needs them.
+ *   stats [B,H,N,2] float32 (m_t, w_t), written; 8-byte aligned.
+ * Other arguments, workspace and errors as aaren_scan_forward_ex (no start
+ * or final state: a sequence that is differentiated starts empty).
+ */
+aaren_status_t aaren_scan_forward_stats(const void *q, const void *K,
+                                        const void *V, void *O, float *stats,
+                                        int64_t B, int64_t H, int64_t N,
+                                        int64_t d, int32_t dtype,
+                                        void *workspace, size_t workspace_bytes,
+                                        void *stream);
+
+/*
+ * aaren_scan_backward -- gradients of the many-to-many output: given the
+ * upstream gradient dO = dL/dO, computes dL/dq, dL/dK and dL/dV in one pass
+ * over K, V, O and dO with O(1) memory per head beyond the inputs (the
+ * memory-efficient-attention review reports its method for differentiation
+ * as well as inference; the Aaren review calls the RNN form exact and
+ * differentiable).  With p_{t,i} = e^{s_i} / sum_{j<=t} e^{s_j}:
+ *     dL/dv_i = sum_{t>=i} p_{t,i} g_t,
+ *     dL/ds_i = sum_{t>=i} p_{t,i} (g_t . v_i - g_t . o_t),
+ *     dL/dq = sum_i dL/ds_i k_i,   dL/dk_i = dL/ds_i q,
+ * computed as suffix sums from the last token back, with the forward's
+ * per-prefix statistics keeping every weight <= 1.
+ *   q [B,H,d], K, V [B,H,N,d]   inputs of the forward (input type)
+ *   O, dO [B,H,N,d]   the forward's output and its gradient (output type)
+ *   stats [B,H,N,2]   from aaren_scan_forward_stats of the same inputs
+ *   dq [B*H,d], dK, dV [B,H,N,d]   gradients, float32, written; they must not
+ *        overlap the inputs or each other
+ *   workspace, workspace_bytes   at least aaren_backward_workspace_bytes
+ *        bytes, 256-byte aligned, or NULL (stream-ordered allocation)
+ * N = 0 writes dq = 0.  Errors: AAREN_ERR_INVALID, AAREN_ERR_UNSUPPORTED,
+ * AAREN_ERR_CUDA, AAREN_ERR_WORKSPACE; device-side waits that give up are
+ * reported by aaren_check().  dL/dq is summed with float32 atomics, so its
+ * last bits may differ between runs.
+ */
+aaren_status_t aaren_scan_backward(const void *q, const void *K, const void *V,
+                                   const void *O, const void *dO,
+                                   const float *stats, float *dq, float *dK,
+                                   float *dV, int64_t B, int64_t H, int64_t N,
+                                   int64_t d, int32_t dtype, void *workspace,
+                                   size_t workspace_bytes, void *stream);
+
+/* Bytes of workspace aaren_scan_backward needs for this shape (0 when N = 0
+ * or B*H = 0; SIZE_MAX when d is unsupported or the shape overflows). */
+size_t aaren_backward_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t d);
+
+/*
  * aaren_scan_reduce -- the many-to-one output: for every head only the last
  * output o_N = sum_{i<=N} e^{s_i} v_i / sum_{i<=N} e^{s_i} and, optionally,
  * the final state (m, u, w); no per-token output is written, so K and V are

@@ -226,13 +226,15 @@ def backward(q, K, V, G):
 
 
 def backward_heads(q, K, V, G, threads=1):
-    """backward() for independent heads: q [BH,d], K/V/G [BH,N,d]."""
+    """backward() for independent heads: q [BH,d], K/V/G [BH,N,d].
+    Returns (dq [BH,d], dK, dV [BH,N,d], ds [BH,N])."""
     q, K, V, G = _f32(q), _f32(K), _f32(V), _f32(G)
     BH, N, d = K.shape
     dq = np.empty((BH, d)); dK = np.empty((BH, N, d)); dV = np.empty((BH, N, d))
+    ds = np.empty((BH, N))
 
     def one(h):
-        dq[h], dK[h], dV[h], _ = backward(q[h], K[h], V[h], G[h])
+        dq[h], dK[h], dV[h], ds[h] = backward(q[h], K[h], V[h], G[h])
 
     if threads <= 1:
         for h in range(BH):
@@ -240,7 +242,7 @@ def backward_heads(q, K, V, G, threads=1):
     else:
         with ThreadPoolExecutor(max_workers=threads) as ex:
             list(ex.map(one, range(BH)))
-    return dq, dK, dV
+    return dq, dK, dV, ds
 
 
 def scan_heads(q, K, V, threads=1, want_O=True):
