@@ -58,9 +58,10 @@ def parse():
     ap.add_argument("--heads", type=int, default=0, help="override H (profiling small cases)")
     ap.add_argument("--tokens", type=int, default=0, help="override N (profiling small cases)")
     ap.add_argument("--out-dtype", default="", choices=["", "bf16", "f32"])
-    ap.add_argument("--op", default="scan", choices=["scan", "reduce"],
+    ap.add_argument("--op", default="scan", choices=["scan", "reduce", "backward"],
                     help="scan: every prefix output (the headline); reduce: the many-to-one "
-                         "form (o_N and the final state only)")
+                         "form (o_N and the final state only); backward: dq, dK, dV of the "
+                         "scan from O, dO and the saved per-prefix statistics")
     return ap.parse_args()
 
 
@@ -317,14 +318,33 @@ def run_ours(args):
     # together process a batch of world * B sequences (weak scaling)
     q, K, V = inputs.batch_inputs(wl, device="cuda", b0=rank * wl.B)
     reduce = args.op == "reduce"
+    backward = args.op == "backward"
     O = torch.empty((wl.B, wl.H, wl.d) if reduce else K.shape, dtype=out_t, device="cuda")
-    ws = (binding.new_reduce_workspace if reduce else binding.new_workspace)(wl.B, wl.H, wl.N, wl.d)
+    if reduce:
+        ws = binding.new_reduce_workspace(wl.B, wl.H, wl.N, wl.d)
+    elif backward:
+        ws = binding.new_backward_workspace(wl.B, wl.H, wl.N, wl.d)
+        # the step's forward (untimed) and an upstream gradient dL/dO ~ N(0, 1)
+        stats = torch.empty(wl.B, wl.H, wl.N, 2, dtype=torch.float32, device="cuda")
+        binding.aaren_scan_forward_stats(q, K, V, O, stats)
+        gwl = inputs.custom(wl.B, wl.H, wl.N, wl.d, dtype=out, seed=wl.seed + 7777)
+        dO = inputs.batch_inputs(gwl, device="cuda", b0=rank * wl.B)[2]
+        g_q = torch.empty(wl.B, wl.H, wl.d, dtype=torch.float32, device="cuda")
+        g_K = torch.empty(K.shape, dtype=torch.float32, device="cuda")
+        g_V = torch.empty(K.shape, dtype=torch.float32, device="cuda")
+    else:
+        ws = binding.new_workspace(wl.B, wl.H, wl.N, wl.d)
     stream = torch.cuda.current_stream()
     in_b = 2 if wl.dtype == "bf16" else 4
     out_b = 2 if out == "bf16" else 4
     elems = wl.heads * wl.N * wl.d
-    # algorithmic bytes: K, V read once (+ O written once for the scan)
-    alg_bytes = elems * (2 * in_b + (0 if reduce else out_b))
+    # algorithmic bytes: K, V read once (+ O written once for the scan); the
+    # backward reads K, V, O, dO and the per-prefix (m, w) once and writes
+    # dK, dV (float32) once
+    if backward:
+        alg_bytes = elems * (2 * in_b + 2 * out_b + 2 * 4) + wl.heads * wl.N * 8
+    else:
+        alg_bytes = elems * (2 * in_b + (0 if reduce else out_b))
     tokens = wl.heads * wl.N
     flush = None
     if elems * 2 * in_b < (1 << 28):                # small workloads sit in L2: flush it
@@ -334,6 +354,9 @@ def run_ours(args):
     def call(q, K, V, O):
         if reduce:
             binding.aaren_scan_reduce(q, K, V, O, workspace=ws, stream=stream)
+        elif backward:
+            binding.aaren_scan_backward(q, K, V, O, dO, stats, g_q, g_K, g_V, workspace=ws,
+                                        stream=stream)
         else:
             binding.aaren_scan_forward_ex(q, K, V, O, workspace=ws, stream=stream)
 
@@ -379,7 +402,11 @@ def run_ours(args):
 
     # end to end through the C ABI with host buffers
     e2e = None
-    if rank == 0 or world > 1:
+    if backward:
+        e2e = {"value": None, "not_measured": "the backward's host copies (K, V, O, dO in; dK, dV "
+                                              "out: 34 GB a step at full size) are not timed; see the "
+                                              "scan's line for the end-to-end figure"}
+    if (rank == 0 or world > 1) and not backward:
         hq = torch.empty(q.shape, dtype=in_t, pin_memory=True)
         hK = torch.empty(K.shape, dtype=in_t, pin_memory=True)
         hV = torch.empty(V.shape, dtype=in_t, pin_memory=True)
@@ -426,7 +453,7 @@ def run_ours(args):
 
     peak, peak_src = measured_peak()
     achieved = alg_bytes / (mean_launch_ms * 1e-3) / 1e9
-    traffic = None if reduce else profiled_traffic(wl, out)
+    traffic = None if (reduce or backward) else profiled_traffic(wl, out)
     line = {
         "metric": METRIC,
         "value": whole_job_rate(tokens, world, step_ms),
@@ -441,7 +468,7 @@ def run_ours(args):
                      "frac": achieved / peak, "traffic": traffic,
                      "algorithmic_bytes_per_launch": alg_bytes, "launch_ms": mean_launch_ms,
                      "peak_source": peak_src,
-                     "kernel": "k_scan_reduce" if reduce else
+                     "kernel": "k_scan_reduce" if reduce else "k_scan_bwd" if backward else
                                ("k_scan_pipe" if wl.dtype == "bf16" else "k_scan_fwd")},
         "cpu_baseline": cpu,
         "e2e": e2e,
