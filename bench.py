@@ -58,10 +58,11 @@ def parse():
     ap.add_argument("--heads", type=int, default=0, help="override H (profiling small cases)")
     ap.add_argument("--tokens", type=int, default=0, help="override N (profiling small cases)")
     ap.add_argument("--out-dtype", default="", choices=["", "bf16", "f32"])
-    ap.add_argument("--op", default="scan", choices=["scan", "reduce", "backward"],
+    ap.add_argument("--op", default="scan", choices=["scan", "reduce", "backward", "step"],
                     help="scan: every prefix output (the headline); reduce: the many-to-one "
                          "form (o_N and the final state only); backward: dq, dK, dV of the "
-                         "scan from O, dO and the saved per-prefix statistics")
+                         "scan from O, dO and the saved per-prefix statistics; step: the "
+                         "one-token update of many streams (the stream workload)")
     return ap.parse_args()
 
 
@@ -480,10 +481,106 @@ def run_ours(args):
     return 0
 
 
+def run_step(args):
+    """The constant-memory one-token update of many streams: every stream of
+    the stream workload (256 x 8 = 2048 streams, d = 64, float32) advances
+    by one token per aaren_step call, for all 4096 tokens.  Timed two ways:
+    plain launches through the binding (each call pays the host launch
+    cost), and the same 4096 calls captured once in a CUDA graph and
+    replayed (the device time of a step).  A step moves 1.6 MB of K, V and
+    O (plus 1.1 MB of state read and written): it is launch-bound."""
+    import torch
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    from attention_prefix_scan_02_b300 import binding, build, inputs
+    build.build()
+    wl = inputs.WORKLOADS["stream"]
+    n, d, T = wl.heads, wl.d, wl.N
+    q, K, V = inputs.batch_inputs(wl, b0=rank * wl.B)
+    qs = q.reshape(n, d).cuda()
+    Ks = K.permute(2, 0, 1, 3).reshape(T, n, d).contiguous().cuda()
+    Vs = V.permute(2, 0, 1, 3).reshape(T, n, d).contiguous().cuda()
+    del K, V
+    Os = torch.empty((T, n, d), dtype=torch.float32, device="cuda")
+    m = torch.empty(n, device="cuda"); u = torch.empty(n, d, device="cuda")
+    w = torch.empty(n, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def sequence():
+        binding.aaren_state_init(m, u, w, stream=stream)
+        for t in range(T):
+            binding.aaren_step(qs, m, u, w, Ks[t], Vs[t], Os[t], stream=stream)
+
+    warmup = max(3, args.warmup)
+    steps = max(1, min(args.steps, 5))
+    for _ in range(warmup):
+        sequence()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True); b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        sequence()
+    b.record(stream)
+    torch.cuda.synchronize()
+    plain_us = a.elapsed_time(b) * 1e3 / (steps * T)
+
+    gs = torch.cuda.Stream()
+    gs.wait_stream(stream)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=gs):
+        binding.aaren_state_init(m, u, w)
+        for t in range(T):
+            binding.aaren_step(qs, m, u, w, Ks[t], Vs[t], Os[t])
+    for _ in range(warmup):
+        g.replay()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        time.sleep(0.3)
+        clocks.begin = time.time()
+        a.record(stream)
+        for _ in range(steps):
+            g.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        clocks.end = time.time()
+    graph_us = a.elapsed_time(b) * 1e3 / (steps * T)
+    if binding.aaren_check() != binding.AAREN_OK:
+        raise SystemExit("device status error in the step benchmark")
+    if rank != 0:
+        return 0
+    step_bytes = n * d * 4 * 3            # k_t, v_t read, o_t written
+    peak, peak_src = measured_peak()
+    line = {
+        "metric": METRIC + " (one-token step of many streams)",
+        "value": world * n / (graph_us * 1e-6), "unit": "head-tokens/s",
+        "n_gpus": world, "steps": steps, "warmup": warmup,
+        "ms_per_step": graph_us * 1e-3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": f"stream: {wl.B} streams x {wl.H} heads = {n} streams, d={d}, "
+                               f"{T} tokens each, f32, seed {wl.seed}", "op": "step",
+                   "l2": "state and one token per stream are L2-resident by design"},
+        "gpu_launches": steps * (T + 1),
+        "step_us": {"cuda_graph": graph_us, "plain_launches": plain_us},
+        "roofline": {"bound": "launch", "achieved": step_bytes / (graph_us * 1e-6) / 1e9,
+                     "peak": peak, "unit": "GB/s", "frac": step_bytes / (graph_us * 1e-6) / 1e9 / peak,
+                     "traffic": None, "algorithmic_bytes_per_launch": step_bytes,
+                     "peak_source": peak_src, "kernel": "k_step"},
+        "e2e": {"value": world * n / (plain_us * 1e-6), "unit": "head-tokens/s",
+                "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0,
+                "path": "plain aaren_step calls through the binding, device-resident tokens"},
+        "clocks": clocks.summary(),
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         return run_reference(args)
+    if args.op == "step":
+        return run_step(args)
     return run_ours(args)
 
 
