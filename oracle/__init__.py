@@ -1,10 +1,11 @@
-"""Float64 oracle for the softmax-attention prefix scan (ctypes wrapper).
+"""Float64 oracle for the softmax-attention prefix scan and the causal
+cos-re-weighted linear-attention scan (ctypes wrapper).
 
 TEST INFRASTRUCTURE ONLY: the tests, the package smoke check and the
 benchmark's CPU-baseline leg are the only callers.  The CUDA library and its
 Python binding never import this package, and this package imports nothing
-from them.  All arithmetic lives in oracle.c (plain sequential C in double);
-this module only converts numpy arrays and calls it.
+from them.  All arithmetic lives in oracle.c (plain sequential C in double)
+and linattn.c; this module only converts numpy arrays and calls them.
 
 Inputs are float32 numpy arrays (bfloat16 data must be widened to float32
 first, which is exact).  Outputs are float64.
@@ -57,6 +58,11 @@ def _bind(path):
     lib.oracle_backward.argtypes = [_f32p, _f32p, _f32p, _f32p, _i64, _i64,
                                     _f64p, _f64p, _f64p, _f64p]
     lib.oracle_backward.restype = ctypes.c_int
+    lib.oracle_la_bruteforce.argtypes = [_f32p, _f32p, _f32p, _i64, _i64, ctypes.c_double, _f64p]
+    lib.oracle_la_bruteforce.restype = None
+    lib.oracle_la_scan.argtypes = [_f32p, _f32p, _f32p, _i64, _i64, ctypes.c_double, _i64,
+                                   _f64p, _f64p, _f64p, _f64p, _f64p, _f64p, _f64p, _f64p, _f64p]
+    lib.oracle_la_scan.restype = ctypes.c_int
     return lib
 
 
@@ -267,6 +273,60 @@ def scan_heads(q, K, V, threads=1, want_O=True):
         with ThreadPoolExecutor(max_workers=threads) as ex:
             list(ex.map(one, range(BH)))
     return O, m, u, w
+
+
+def _opt64(a):
+    return None if a is None else _p64(a)
+
+
+def la_bruteforce(Q, K, V, M):
+    """Causal cos-re-weighted linear attention from its definition, O(N^2 d):
+    o_i = sum_{j<=i} s_ij v_j / sum_{j<=i} s_ij with
+    s_ij = relu(Q_i) . relu(K_j) cos(pi/2 (i - j) / M).  Returns O [N,d]."""
+    Q, K, V = _f32(Q), _f32(K), _f32(V)
+    N, d = K.shape
+    O = np.empty((N, d))
+    _load().oracle_la_bruteforce(_p32(Q), _p32(K), _p32(V), N, d, float(M), _p64(O))
+    return O
+
+
+def la_scan(Q, K, V, M, init=None, pos0=0, want_O=True):
+    """The same output by the decomposed prefix sums, O(N d^2).  init =
+    (Sc, Ss, zc, zs) continues a scan whose last token had position pos0.
+    Returns (O [N,d] or None, (Sc [d,d], Ss [d,d], zc [d], zs [d]))."""
+    Q, K, V = _f32(Q), _f32(K), _f32(V)
+    N, d = K.shape
+    O = np.empty((N, d)) if want_O else None
+    Sc = np.empty((d, d)); Ss = np.empty((d, d)); zc = np.empty(d); zs = np.empty(d)
+    ini = [None] * 4 if init is None else [_f64(x) for x in init]
+    if _load().oracle_la_scan(_p32(Q), _p32(K), _p32(V), N, d, float(M), int(pos0),
+                              *(_opt64(x) for x in ini), _opt64(O), _p64(Sc), _p64(Ss),
+                              _p64(zc), _p64(zs)) != 0:
+        raise MemoryError("oracle_la_scan: allocation failed")
+    return O, (Sc, Ss, zc, zs)
+
+
+def la_heads(Q, K, V, M, threads=1, want_O=True):
+    """la_scan() for independent heads: Q/K/V [BH,N,d].  Returns (O [BH,N,d]
+    or None, (Sc [BH,d,d], Ss [BH,d,d], zc [BH,d], zs [BH,d]))."""
+    Q, K, V = _f32(Q), _f32(K), _f32(V)
+    BH, N, d = K.shape
+    O = np.empty((BH, N, d)) if want_O else None
+    Sc = np.empty((BH, d, d)); Ss = np.empty((BH, d, d)); zc = np.empty((BH, d))
+    zs = np.empty((BH, d))
+
+    def one(h):
+        o, (Sc[h], Ss[h], zc[h], zs[h]) = la_scan(Q[h], K[h], V[h], M, want_O=want_O)
+        if want_O:
+            O[h] = o
+
+    if threads <= 1:
+        for h in range(BH):
+            one(h)
+    else:
+        with ThreadPoolExecutor(max_workers=threads) as ex:
+            list(ex.map(one, range(BH)))
+    return O, (Sc, Ss, zc, zs)
 
 
 def lib_path():

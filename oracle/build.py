@@ -1,4 +1,4 @@
-"""Compile the float64 oracle (oracle.c) into oracle/liboracle.so.
+"""Compile the float64 oracle (oracle.c, linattn.c) into oracle/liboracle.so.
 
 Test infrastructure: the oracle is built so the tests and the benchmark's
 CPU-baseline leg can call it; the CUDA library never links or loads it.
@@ -10,18 +10,18 @@ import os
 import subprocess
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-SRC = os.path.join(HERE, "oracle.c")
+SRCS = [os.path.join(HERE, "oracle.c"), os.path.join(HERE, "linattn.c")]
 LIB = os.path.join(HERE, "liboracle.so")
 
 
 def build(force: bool = False) -> str:
-    """Build liboracle.so if it is missing or older than oracle.c; return its path."""
+    """Build liboracle.so if it is missing or older than its sources; return its path."""
     if (not force and os.path.exists(LIB)
-            and os.path.getmtime(LIB) >= os.path.getmtime(SRC)):
+            and all(os.path.getmtime(LIB) >= os.path.getmtime(s) for s in SRCS)):
         return LIB
     tmp = LIB + f".tmp{os.getpid()}"
     cmd = ["gcc", "-O2", "-std=c99", "-fPIC", "-shared", "-fno-fast-math",
-           "-o", tmp, SRC, "-lm"]
+           "-o", tmp, *SRCS, "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, LIB)
     return LIB

@@ -37,6 +37,17 @@ Differentiation (gradients of L = sum_t g_t . o_t):
   log-sum-exp      lse_t (running form) equals scipy.special.logsumexp of
                    every prefix and the per-prefix direct form
   large scores     |s| in the hundreds: the backward stays finite and agrees
+Causal cos-re-weighted linear attention (cosFormer):
+  worked example   hand-derived outputs and final state, exact in a + b sqrt3
+                   (tests/golden/cosformer_worked_example.txt)
+  definition       the decomposed prefix sums equal the O(N^2 d) definition
+  ReLU linear att. M -> infinity gives causal ReLU linear attention written
+                   with numpy matrix products
+  prefix means     equal similarities, M -> infinity: cumsum(V) / i
+  invariances      query-row and key scaling, ReLU of negative coordinates,
+                   value shift, causality, o_1 = v_1, box bounds
+  zero query       a query with no positive coordinate gives o_i = 0
+  continuation     scanning [A; B] equals scanning B from A's state
 """
 import os
 from fractions import Fraction
@@ -56,6 +67,31 @@ def _rng(seed):
 def _rel(a, b):
     a, b = np.asarray(a, np.float64), np.asarray(b, np.float64)
     return float(np.max(np.abs(a - b)) / max(1e-300, float(np.max(np.abs(b)))))
+
+
+def read_fixture_r3(name):
+    """Like read_fixture, but keys ending in _r3 hold a,b pairs (a + b*sqrt3),
+    returned as float64 arrays; other keys as float64 arrays of fractions."""
+    out = {}
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            key, rest = line.split(":", 1)
+            key = key.strip()
+            rows = []
+            for r in rest.split("|"):
+                if key.endswith("_r3"):
+                    vals = []
+                    for x in r.split():
+                        a, b = x.split(",")
+                        vals.append(float(Fraction(a)) + float(Fraction(b)) * np.sqrt(3.0))
+                    rows.append(vals)
+                else:
+                    rows.append([float(Fraction(x)) for x in r.split()])
+            out[key] = np.array(rows, dtype=np.float64)
+    return out
 
 
 def read_fixture(name):
@@ -384,11 +420,138 @@ def pin_backward_large_scores():
         assert _rel(a, b) < 1e-11
 
 
+# ---------------------------------------------------------------------------
+# Causal cos-re-weighted linear attention (cosFormer section of the LG AI
+# Research "Efficient Transformer" review).
+# ---------------------------------------------------------------------------
+
+def _la_inputs(seed, N, d, neg=True):
+    r = _rng(seed)
+    Q = r.standard_normal((N, d)).astype(np.float32)
+    K = r.standard_normal((N, d)).astype(np.float32)
+    V = r.standard_normal((N, d)).astype(np.float32)
+    if not neg:
+        Q, K = np.abs(Q), np.abs(K)
+    return Q, K, V
+
+
+def pin_la_worked_example():
+    fx = read_fixture_r3("cosformer_worked_example.txt")
+    M = float(fx["M"][0][0])
+    Q, K, V = (fx[k].astype(np.float32) for k in ("Q", "K", "V"))
+    num, den = fx["num_r3"], fx["den_r3"][:, 0]
+    want = np.where(den[:, None] != 0, num / np.where(den == 0, 1, den)[:, None], 0.0)
+    Ob = oracle.la_bruteforce(Q, K, V, M)
+    O, (Sc, Ss, zc, zs) = oracle.la_scan(Q, K, V, M)
+    assert np.max(np.abs(Ob - want)) < 1e-14, (Ob, want)
+    assert np.max(np.abs(O - want)) < 1e-13, (O, want)
+    assert np.max(np.abs(zc - fx["zc_r3"][0])) < 1e-13 and np.max(np.abs(zs - fx["zs_r3"][0])) < 1e-13
+    assert np.max(np.abs(Sc - fx["Sc_r3"])) < 1e-13, (Sc, fx["Sc_r3"])
+    assert np.max(np.abs(Ss - fx["Ss_r3"])) < 1e-13, (Ss, fx["Ss_r3"])
+
+
+def pin_la_scan_equals_definition():
+    """The decomposed prefix sums equal the definition (two different
+    computations: cos of the difference vs the cosine sum formula)."""
+    for seed, N, d, Mf in ((1, 1, 4, 1.0), (2, 7, 3, 1.0), (3, 64, 16, 1.0), (4, 200, 8, 2.5),
+                           (5, 150, 32, 40.0)):
+        Q, K, V = _la_inputs(seed, N, d)
+        M = Mf * N
+        Ob = oracle.la_bruteforce(Q, K, V, M)
+        O, _ = oracle.la_scan(Q, K, V, M)
+        assert _rel(O, Ob) < 1e-12, (N, d, _rel(O, Ob))
+
+
+def pin_la_relu_linear_attention():
+    """M -> infinity removes the re-weighting (every cos is 1): the output is
+    causal linear attention with the ReLU feature map, written with numpy
+    matrix products (the masked similarity matrix, normalised by its row
+    sums)."""
+    for seed, N, d in ((6, 50, 8), (7, 120, 16)):
+        Q, K, V = _la_inputs(seed, N, d)
+        Qp, Kp = np.maximum(Q.astype(np.float64), 0), np.maximum(K.astype(np.float64), 0)
+        P = np.tril(Qp @ Kp.T)
+        rs = P.sum(axis=1, keepdims=True)
+        want = np.where(rs > 0, (P @ V.astype(np.float64)) / np.where(rs > 0, rs, 1), 0.0)
+        for got in (oracle.la_bruteforce(Q, K, V, 1e300), oracle.la_scan(Q, K, V, 1e300)[0]):
+            assert _rel(got, want) < 1e-12, _rel(got, want)
+
+
+def pin_la_prefix_means():
+    """All similarities equal and M -> infinity: o_i is the mean of v_1..v_i."""
+    N, d = 40, 5
+    Q = np.full((N, d), 0.5, np.float32)
+    K = np.full((N, d), 2.0, np.float32)
+    V = _la_inputs(8, N, d)[2]
+    want = np.cumsum(V.astype(np.float64), axis=0) / np.arange(1, N + 1)[:, None]
+    for got in (oracle.la_bruteforce(Q, K, V, 1e300), oracle.la_scan(Q, K, V, 1e300)[0]):
+        assert _rel(got, want) < 1e-13
+
+
+def pin_la_invariances():
+    """Scaling a query row or all keys by c > 0 (powers of two, so the inputs
+    stay exact) leaves O unchanged; negative
+    coordinates of Q and K act as zeros (the ReLU map); adding a constant
+    vector to every value adds it to every output; o_i does not depend on
+    tokens after i; o_1 = v_1; each o_i lies in the box spanned by v_1..v_i."""
+    N, d = 80, 12
+    Q, K, V = _la_inputs(9, N, d)
+    M = float(N)
+    O, _ = oracle.la_scan(Q, K, V, M)
+    c = np.float32(2.0) ** (np.arange(N) % 7 - 3).astype(np.float32)[:, None]   # exact scalings
+    assert _rel(oracle.la_scan(Q * c, K, V, M)[0], O) < 1e-13
+    assert _rel(oracle.la_scan(Q, K * np.float32(4.0), V, M)[0], O) < 1e-13
+    Qn = np.where(Q > 0, Q, np.float32(-7.0)); Kn = np.where(K > 0, K, np.float32(-0.5))
+    assert _rel(oracle.la_scan(Qn, Kn, V, M)[0], O) < 1e-15
+    Vq = (np.round(V * 1024) / 1024).astype(np.float32)           # dyadic: V + shift stays exact
+    shift = np.arange(-5, d - 5).astype(np.float32)
+    O = oracle.la_scan(Q, K, Vq, M)[0]
+    Os = oracle.la_scan(Q, K, Vq + shift, M)[0]
+    sim = np.tril(np.maximum(Q.astype(np.float64), 0) @ np.maximum(K.astype(np.float64), 0).T)
+    live = np.any(sim > 0, axis=1)          # rows with a non-zero denominator
+    assert np.max(np.abs(Os[live] - (O[live] + shift))) < 1e-12
+    O, V = oracle.la_scan(Q, K, V, M)[0], V
+    K2, V2 = K.copy(), V.copy()
+    K2[50:] = _la_inputs(10, N - 50, d)[1]; V2[50:] = 9.0
+    assert np.max(np.abs(oracle.la_scan(Q, K2, V2, M)[0][:50] - O[:50])) == 0.0
+    assert np.max(np.abs(oracle.la_bruteforce(Q, K2, V2, M)[:50] - oracle.la_bruteforce(Q, K, V, M)[:50])) == 0.0
+    if np.dot(np.maximum(Q[0], 0), np.maximum(K[0], 0)) > 0:
+        assert np.max(np.abs(O[0] - V[0])) < 1e-15
+    lo = np.minimum.accumulate(V.astype(np.float64), axis=0)
+    hi = np.maximum.accumulate(V.astype(np.float64), axis=0)
+    assert np.all(O[live] >= lo[live] - 1e-12) and np.all(O[live] <= hi[live] + 1e-12)
+
+
+def pin_la_zero_query():
+    """A query with no positive coordinate has zero similarity to every key:
+    its output is 0 (the reading for an empty weighted average)."""
+    Q, K, V = _la_inputs(11, 30, 6)
+    Q[[0, 7, 29]] = -np.abs(Q[[0, 7, 29]])
+    for got in (oracle.la_bruteforce(Q, K, V, 30.0), oracle.la_scan(Q, K, V, 30.0)[0]):
+        assert np.all(got[[0, 7, 29]] == 0.0) and np.all(np.isfinite(got))
+
+
+def pin_la_continuation():
+    """Scanning [A; B] equals scanning B from A's final state with positions
+    continued (and both final states agree)."""
+    N, d, cut = 90, 10, 37
+    Q, K, V = _la_inputs(12, N, d)
+    M = float(N)
+    O, st = oracle.la_scan(Q, K, V, M)
+    _, stA = oracle.la_scan(Q[:cut], K[:cut], V[:cut], M, want_O=False)
+    OB, stB = oracle.la_scan(Q[cut:], K[cut:], V[cut:], M, init=stA, pos0=cut)
+    assert _rel(OB, O[cut:]) < 1e-13
+    for a, b in zip(stB, st):
+        assert _rel(a, b) < 1e-13
+
+
 ALL_PINS = [
     pin_worked_example, pin_bruteforce, pin_last_row, pin_scores, pin_shift,
     pin_equal_scores, pin_hillis_steele, pin_operator_laws, pin_first_output,
     pin_one_hot, pin_bounds, pin_long_double, pin_large_scores, pin_continuation,
     pin_running_sum, pin_backward_finite_differences, pin_backward_suffix_sums,
     pin_backward_shift, pin_backward_one_token, pin_backward_equal_scores, pin_lse,
-    pin_backward_large_scores,
+    pin_backward_large_scores, pin_la_worked_example, pin_la_scan_equals_definition,
+    pin_la_relu_linear_attention, pin_la_prefix_means, pin_la_invariances, pin_la_zero_query,
+    pin_la_continuation,
 ]

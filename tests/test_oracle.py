@@ -59,16 +59,47 @@ MUTANTS = {
 }
 
 
-@pytest.mark.parametrize("name", sorted(MUTANTS))
-def test_planted_mistake_fails_a_pin(name, tmp_path):
-    src = open(oracle_build.SRC).read()
-    old, new = MUTANTS[name]
-    assert src.count(old) == 1, f"mutant {name} no longer matches oracle.c"
-    csrc = tmp_path / "mutant.c"
-    csrc.write_text(src.replace(old, new))
+# The same for linattn.c (the causal cos-re-weighted linear attention).
+LA_MUTANTS = {
+    "la_no_relu_k": ("kp[a] = relu_d(K[t * d + a]);", "kp[a] = (double)K[t * d + a];"),
+    "la_brute_no_relu_q": ("dot += relu_d(Q[i * d + c]) * relu_d(K[j * d + c]);",
+                           "dot += (double)Q[i * d + c] * relu_d(K[j * d + c]);"),
+    "la_brute_weight_sum": ("double s = dot * cos(hp * (double)(i - j) / M);",
+                            "double s = dot * cos(hp * (double)(i + j) / M);"),
+    "la_brute_exclusive": ("for (int64_t j = 0; j <= i; ++j) {", "for (int64_t j = 0; j < i; ++j) {"),
+    "la_sin_sign": ("num += qp[a] * ct * Sc[a * d + b] + qp[a] * st * Ss[a * d + b];",
+                    "num += qp[a] * ct * Sc[a * d + b] - qp[a] * st * Ss[a * d + b];"),
+    "la_den_dropped_sin": ("den += qp[a] * ct * zc[a] + qp[a] * st * zs[a];",
+                           "den += qp[a] * ct * zc[a];"),
+    "la_state_transposed": ("Sc[a * d + b] += kc * v;", "Sc[b * d + a] += kc * v;"),
+    "la_position_zero_based": ("double pos = (double)(pos0 + t + 1);",
+                               "double pos = (double)(pos0 + t);"),
+    "la_zero_den": ("O[t * d + b] = den != 0.0 ? num / den : 0.0;", "O[t * d + b] = num / den;"),
+}
+
+
+def _all_mutants():
+    for name in sorted(MUTANTS):
+        yield name, "oracle.c"
+    for name in sorted(LA_MUTANTS):
+        yield name, "linattn.c"
+
+
+@pytest.mark.parametrize("name,fname", list(_all_mutants()))
+def test_planted_mistake_fails_a_pin(name, fname, tmp_path):
+    old, new = (MUTANTS if fname == "oracle.c" else LA_MUTANTS)[name]
+    srcs = []
+    for path in oracle_build.SRCS:
+        text = open(path).read()
+        if os.path.basename(path) == fname:
+            assert text.count(old) == 1, f"mutant {name} no longer matches {fname}"
+            text = text.replace(old, new)
+        csrc = tmp_path / os.path.basename(path)
+        csrc.write_text(text)
+        srcs.append(str(csrc))
     so = tmp_path / "libmutant.so"
     subprocess.run(["gcc", "-O2", "-std=c99", "-fPIC", "-shared", "-o", str(so),
-                    str(csrc), "-lm"], check=True)
+                    *srcs, "-lm"], check=True)
     failed = []
     with oracle.using_library(str(so)):
         for pin in oracle_pins.ALL_PINS:
@@ -82,7 +113,7 @@ def test_planted_mistake_fails_a_pin(name, tmp_path):
 def test_oracle_is_independent_of_the_cuda_path():
     """The oracle shares no code with the CUDA library: no include of the
     library's headers, no import of the package."""
-    here = os.path.dirname(oracle_build.SRC)
+    here = os.path.dirname(oracle_build.SRCS[0])
     for fn in os.listdir(here):
         if fn.endswith((".c", ".h", ".py")):
             text = open(os.path.join(here, fn)).read()
