@@ -36,6 +36,7 @@ EXPORTS = (
     "aaren_abi_version", "aaren_debug_set_fault", "aaren_scan_chunk_tokens",
     "aaren_scan_forward_noalloc", "aaren_scan_reduce", "aaren_reduce_workspace_bytes",
     "aaren_scan_forward_stats", "aaren_scan_backward", "aaren_backward_workspace_bytes",
+    "aaren_linattn_forward",
 )
 
 # size of the fixed device scratch of aaren_scan_forward_noalloc (include/aaren.h)
@@ -101,6 +102,9 @@ def load(path: str | None = None):
     lib.aaren_scan_backward.restype = _i32
     lib.aaren_backward_workspace_bytes.argtypes = [_i64, _i64, _i64, _i64]
     lib.aaren_backward_workspace_bytes.restype = ctypes.c_size_t
+    lib.aaren_linattn_forward.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, ctypes.c_double,
+                                          _i64, _i32, _vp, _vp, _vp, _vp, _vp]
+    lib.aaren_linattn_forward.restype = _i32
     if path is None:
         _lib = lib
     return lib
@@ -411,3 +415,49 @@ def new_backward_workspace(B, H, N, d, device="cuda"):
 def new_workspace(B, H, N, d, device="cuda"):
     nbytes = aaren_scan_workspace_bytes(B, H, N, d)
     return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+
+
+def aaren_linattn_forward(Q, K, V, O, M, pos0=0, S_in=None, z_in=None, S_out=None, z_out=None,
+                          stream=None):
+    """Causal cos-re-weighted linear attention (include/aaren.h):
+    Q, K, V [B,H,N,64] bfloat16, O [B,H,N,64] bfloat16 or float32; states
+    S [B,H,2,64,64], z [B,H,2,64] float32 (or None)."""
+    _check_cuda(Q, K, V, O, S_in, z_in, S_out, z_out)
+    if Q.dim() != 4 or Q.shape != K.shape or K.shape != V.shape or O.shape != K.shape:
+        raise ValueError("Q, K, V, O must all be [B, H, N, d]")
+    if not (Q.dtype == K.dtype == V.dtype):
+        raise ValueError("Q, K, V must share a dtype")
+    B, H, N, d = K.shape
+    for S, z in ((S_in, z_in), (S_out, z_out)):
+        if (S is None) != (z is None):
+            raise ValueError("a state is given as both of (S, z) or neither")
+        if S is not None:
+            if S.dtype != torch.float32 or z.dtype != torch.float32:
+                raise ValueError("state tensors are float32")
+            if S.numel() != B * H * 2 * d * d or z.numel() != B * H * 2 * d:
+                raise ValueError("state shapes must be S [B,H,2,d,d], z [B,H,2,d]")
+    rc = load().aaren_linattn_forward(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), B, H, N, d, float(M),
+                                      int(pos0), dtype_code(K.dtype, O.dtype), _ptr(S_in),
+                                      _ptr(z_in), _ptr(S_out), _ptr(z_out), _stream_handle(stream))
+    _raise(rc, "aaren_linattn_forward")
+    return O
+
+
+def linattn_forward(Q, K, V, M=None, out_dtype=None, init=None, pos0=0, return_state=False,
+                    stream=None):
+    """Allocate O (and the final state when asked) and run
+    aaren_linattn_forward.  M defaults to the sequence length pos0 + N
+    (at least 1).
+    Returns O, or (O, (S, z))."""
+    out_dtype = out_dtype or K.dtype
+    B, H, N, d = K.shape
+    M = float(max(pos0 + N, 1)) if M is None else float(M)
+    O = torch.empty(K.shape, dtype=out_dtype, device=K.device)
+    S_in = z_in = S_out = z_out = None
+    if init is not None:
+        S_in, z_in = init
+    if return_state:
+        S_out = torch.empty(B, H, 2, d, d, dtype=torch.float32, device=K.device)
+        z_out = torch.empty(B, H, 2, d, dtype=torch.float32, device=K.device)
+    aaren_linattn_forward(Q, K, V, O, M, pos0, S_in, z_in, S_out, z_out, stream)
+    return (O, (S_out, z_out)) if return_state else O

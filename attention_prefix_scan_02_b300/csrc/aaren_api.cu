@@ -1,11 +1,13 @@
 // aaren_api.cu -- host side of libaaren: argument checks, tile selection,
 // workspace layout, launches and the device status word.  The operation and
 // the conventions are documented in include/aaren.h.
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <atomic>
 #include <climits>
+#include <cmath>
 #include <cstdint>
 #include <cstdlib>
 
@@ -16,6 +18,7 @@
 #include "reduce_kernel.cuh"
 #include "bwd_kernel.cuh"
 #include "step_kernel.cuh"
+#include "linattn_kernel.cuh"
 
 namespace aaren {
 
@@ -404,12 +407,116 @@ aaren_status_t dispatch_reduce(const ReduceParams &p, int64_t P_max, int64_t d, 
     }
 }
 
+// ---- causal cos-re-weighted linear attention -------------------------------
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// The driver's tensor-map encoder, looked up once through the runtime.
+EncodeTiledFn encode_tiled()
+{
+    static const EncodeTiledFn fn = [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return static_cast<EncodeTiledFn>(nullptr);
+        return reinterpret_cast<EncodeTiledFn>(f);
+    }();
+    return fn;
+}
+
+// [BH, N, 64] bfloat16 viewed as a 3-D tensor; boxes of 128 tokens x 64,
+// 128-byte swizzle, rows past N read as zero.
+bool linattn_map(CUtensorMap *m, const void *base, int64_t BH, int64_t N)
+{
+    const EncodeTiledFn enc = encode_tiled();
+    if (enc == nullptr) return false;
+    const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH)};
+    const cuuint64_t strides[2] = {64 * 2, static_cast<cuuint64_t>(N) * 64 * 2};
+    const cuuint32_t box[3] = {64, la::C, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+static_assert(la::kSmemBytes <= 232448, "linear-attention tile exceeds the opt-in shared memory of a CTA");
+
+template <typename Tout>
+aaren_status_t launch_linattn(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                              const la::Params &p, cudaStream_t st)
+{
+    static bool configured = false;
+    if (!configured) {
+        if (cudaFuncSetAttribute(la::k_linattn<Tout>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 la::kSmemBytes) != cudaSuccess)
+            return AAREN_ERR_CUDA;
+        configured = true;
+    }
+    const int64_t grid = p.BH < sm_count() ? p.BH : sm_count();
+    la::k_linattn<Tout><<<static_cast<unsigned>(grid), la::kThreads, la::kSmemBytes, st>>>(tq, tk, tv, p);
+    return cudaGetLastError() == cudaSuccess ? AAREN_OK : AAREN_ERR_CUDA;
+}
+
 }  // namespace
 }  // namespace aaren
 
 using namespace aaren;
 
 extern "C" {
+
+aaren_status_t aaren_linattn_forward(const void *Q, const void *K, const void *V, void *O, int64_t B,
+                                     int64_t H, int64_t N, int64_t d, double M, int64_t pos0,
+                                     int32_t dtype, const float *S_in, const float *z_in, float *S_out,
+                                     float *z_out, void *stream)
+{
+    if (B < 0 || H < 0 || N < 0 || d <= 0 || pos0 < 0) return AAREN_ERR_INVALID;
+    if (!(M > 0.0) || !std::isfinite(M)) return AAREN_ERR_INVALID;
+    if ((S_in == nullptr) != (z_in == nullptr) || (S_out == nullptr) != (z_out == nullptr))
+        return AAREN_ERR_INVALID;
+    if (d != la::D) return AAREN_ERR_UNSUPPORTED;
+    if (dtype != AAREN_BF16 && dtype != AAREN_BF16_F32OUT) return AAREN_ERR_UNSUPPORTED;
+    int64_t BH, tok, elems;
+    if (!mul_ok(B, H, &BH) || !mul_ok(BH, N, &tok) || !mul_ok(tok, d, &elems)) return AAREN_ERR_INVALID;
+    if (N > INT32_MAX - la::C || BH > INT32_MAX) return AAREN_ERR_INVALID;   // TMA coordinates are 32-bit
+    if (S_in != nullptr && (!aligned(S_in, 16) || !aligned(z_in, 4))) return AAREN_ERR_INVALID;
+    if (S_out != nullptr && (!aligned(S_out, 16) || !aligned(z_out, 4))) return AAREN_ERR_INVALID;
+    if (BH == 0) return AAREN_OK;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const size_t s_bytes = size_t(BH) * 2 * 64 * 64 * sizeof(float), z_bytes = size_t(BH) * 2 * 64 * sizeof(float);
+    if (N == 0) {   // nothing to scan: the final state is the starting state
+        if (S_out == nullptr) return AAREN_OK;
+        const bool ok = (S_in != nullptr)
+                            ? cudaMemcpyAsync(S_out, S_in, s_bytes, cudaMemcpyDeviceToDevice, st) == cudaSuccess &&
+                                  cudaMemcpyAsync(z_out, z_in, z_bytes, cudaMemcpyDeviceToDevice, st) == cudaSuccess
+                            : cudaMemsetAsync(S_out, 0, s_bytes, st) == cudaSuccess &&
+                                  cudaMemsetAsync(z_out, 0, z_bytes, st) == cudaSuccess;
+        return ok ? AAREN_OK : AAREN_ERR_CUDA;
+    }
+    if (Q == nullptr || K == nullptr || V == nullptr || O == nullptr) return AAREN_ERR_INVALID;
+    if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(O, 16)) return AAREN_ERR_INVALID;
+    const size_t in_b = size_t(elems) * 2, out_b = size_t(elems) * out_elem_bytes(dtype);
+    if (overlaps(O, out_b, Q, in_b) || overlaps(O, out_b, K, in_b) || overlaps(O, out_b, V, in_b))
+        return AAREN_ERR_INVALID;
+    CUtensorMap tq, tk, tv;
+    if (!linattn_map(&tq, Q, BH, N) || !linattn_map(&tk, K, BH, N) || !linattn_map(&tv, V, BH, N))
+        return AAREN_ERR_CUDA;
+    unsigned *status = nullptr;
+    if (cudaGetSymbolAddress(reinterpret_cast<void **>(&status), g_status) != cudaSuccess) return AAREN_ERR_CUDA;
+    la::Params p;
+    p.O = O;
+    p.S_in = S_in; p.z_in = z_in; p.S_out = S_out; p.z_out = z_out;
+    p.BH = BH; p.N = N; p.pos0 = pos0;
+    p.inv_2M = 1.0 / (2.0 * M);
+    p.status = status;
+    p.wait_limit_ns = g_wait_limit_ns.load();
+    return dtype == AAREN_BF16 ? launch_linattn<__nv_bfloat16>(tq, tk, tv, p, st)
+                               : launch_linattn<float>(tq, tk, tv, p, st);
+}
 
 size_t aaren_scan_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t d)
 {

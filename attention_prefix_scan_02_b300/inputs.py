@@ -28,6 +28,10 @@ Workloads (name -> shape and value recipe):
               per head drawn once (stream index 0 of the q stream) and shared
               by all 256 streams, as a learned query is; K, V ~ N(0,1) per
               (stream, head).
+  linattn     B=64, H=16, N=2048, d=64, bf16 storage, seed 5: the causal
+              linear-attention (cosFormer) workload, one query per token:
+              Q, K, V ~ N(0,1), each [N, d] per head (Q drawn like K from the
+              q stream).  Re-weighting length M = N.
 """
 from __future__ import annotations
 
@@ -51,7 +55,7 @@ class Workload:
     d: int
     dtype: str   # storage dtype of q, K, V: "f32" or "bf16"
     seed: int
-    kind: str    # "normal", "stress" or "stream"
+    kind: str    # "normal", "stress", "stream" or "tokens" (a query per token)
 
     @property
     def heads(self) -> int:
@@ -64,6 +68,7 @@ WORKLOADS = {
     "stress": Workload("stress", 4, 8, 16384, 64, "f32", 2, "stress"),
     "long": Workload("long", 1, 16, 1 << 20, 128, "bf16", 3, "normal"),
     "stream": Workload("stream", 256, 8, 4096, 64, "f32", 4, "stream"),
+    "linattn": Workload("linattn", 64, 16, 2048, 64, "bf16", 5, "tokens"),
 }
 
 
@@ -165,3 +170,37 @@ def batch_inputs(wl: Workload, device=None, threads: int | None = None, b0: int 
                 K[b, h].copy_(torch.from_numpy(Kh).to(tdt))
                 V[b, h].copy_(torch.from_numpy(Vh).to(tdt))
     return q, K, V
+
+
+def head_token_inputs(wl: Workload, b: int, h: int):
+    """(Q [N, d], K [N, d], V [N, d]) of head (b, h) for workloads with one
+    query per token, float32 numpy holding the stored values."""
+    Q = _normal_rows(wl.seed, TENSOR_Q, b, h, wl.N, wl.d)
+    K = _normal_rows(wl.seed, TENSOR_K, b, h, wl.N, wl.d)
+    V = _normal_rows(wl.seed, TENSOR_V, b, h, wl.N, wl.d)
+    if wl.dtype == "bf16":
+        Q, K, V = round_bf16(Q), round_bf16(K), round_bf16(V)
+    return Q, K, V
+
+
+def token_inputs(wl: Workload, device=None, threads: int | None = None, b0: int = 0):
+    """Q, K, V [B, H, N, d] torch tensors in the storage dtype (one query per
+    token); batch entries b0 .. b0 + B - 1 of the recipe."""
+    import torch
+    tdt = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
+    dev = torch.device("cpu") if device is None else torch.device(device)
+    out = [torch.empty((wl.B, wl.H, wl.N, wl.d), dtype=tdt, device=dev) for _ in range(3)]
+    threads = threads or default_threads()
+
+    def one(bh):
+        b, h = divmod(bh, wl.H)
+        return bh, head_token_inputs(wl, b0 + b, h)
+
+    workers = min(threads, max(1, wl.heads))
+    with ThreadPoolExecutor(max_workers=workers) as ex:
+        for w0 in range(0, wl.heads, workers):
+            for bh, arrs in ex.map(one, range(w0, min(wl.heads, w0 + workers))):
+                b, h = divmod(bh, wl.H)
+                for t, a in zip(out, arrs):
+                    t[b, h].copy_(torch.from_numpy(a).to(tdt))
+    return tuple(out)

@@ -237,6 +237,46 @@ aaren_status_t aaren_step(const void *q, float *m, float *u, float *w,
                           int64_t n, int64_t d, int32_t dtype, void *stream);
 
 /*
+ * aaren_linattn_forward -- causal cos-re-weighted linear attention of every
+ * head (LG AI Research blog "[ICLR 2022] Part 1: Efficient Transformer",
+ * section "cosFormer"): with Q' = ReLU(Q), K' = ReLU(K),
+ *
+ *     s_ij = (Q'_i . K'_j) cos(pi/2 * (i - j) / M)
+ *     o_i  = sum_{j<=i} s_ij v_j / sum_{j<=i} s_ij      (0 where the sum is 0)
+ *
+ * computed as a prefix scan whose state is the section's key-first sums
+ * split by the cosine sum formula: S^cos = sum_j cos(pi j/2M) K'_j^T v_j,
+ * S^sin likewise with sin, z^cos = sum_j cos(pi j/2M) K'_j, z^sin likewise.
+ * Positions j are 1-based and continue from pos0 (the position of the token
+ * before the first one of this call), so a long sequence can be processed in
+ * pieces: pass the previous call's final state and pos0 = tokens so far.
+ *   Q, K, V [B,H,N,d]   bfloat16 queries (one per token), keys, values
+ *   O       [B,H,N,d]   written: bfloat16 (AAREN_BF16) or float32
+ *                        (AAREN_BF16_F32OUT); AAREN_F32 is UNSUPPORTED
+ *   d       64 only (else AAREN_ERR_UNSUPPORTED)
+ *   M       re-weighting length, finite and > 0 (cosFormer takes the
+ *           sequence length; M >= pos0 + N - 1 keeps every weight >= 0)
+ *   S_in, z_in    starting state, float32 [B,H,2,64,64] (index 0 = cos, 1 =
+ *           sin; row = key coordinate, column = value coordinate) and
+ *           [B,H,2,64]; both NULL = the zero state.  16- and 4-byte aligned.
+ *   S_out, z_out  final state in the same layout, or both NULL.  May not
+ *           alias S_in / z_in of other heads (the same head in place is fine).
+ * Arithmetic: float32 accumulation on the tensor cores; every operand the
+ * method rounds (the intra-chunk weights, the position-weighted keys, the
+ * state) is carried as a bfloat16 pair hi + lo, so the result is float32
+ * accurate.  N = 0 copies the starting state to the final state (or zeroes
+ * it).  Errors: AAREN_ERR_INVALID for negative sizes, pos0 < 0, M not finite
+ * and positive, null / misaligned pointers, one of a state pair missing, O
+ * overlapping Q, K or V, N or B*H beyond 2^31 - 129; AAREN_ERR_CUDA when the
+ * driver's tensor-map encoder is unavailable or a launch fails; device
+ * waits that give up are reported by aaren_check().
+ */
+aaren_status_t aaren_linattn_forward(const void *Q, const void *K, const void *V, void *O,
+                                     int64_t B, int64_t H, int64_t N, int64_t d, double M,
+                                     int64_t pos0, int32_t dtype, const float *S_in,
+                                     const float *z_in, float *S_out, float *z_out, void *stream);
+
+/*
  * aaren_check -- synchronise `stream`, then report and clear the device
  * status word of the current device (one word per device, shared by every
  * stream and call: a failure on any stream shows up in the next check).

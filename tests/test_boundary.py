@@ -151,3 +151,33 @@ def test_reduce_workspace_and_argument_checks(lib):
     # no heads: nothing to do
     assert lib.aaren_scan_reduce(n, n, n, fake, 0, 4, 8, 64, 0, n, n, n, n, n, n, n, 0,
                                  n) == binding.AAREN_OK
+
+
+def test_linattn_argument_checks(lib):
+    """aaren_linattn_forward rejects bad arguments before any CUDA call."""
+    f = lib.aaren_linattn_forward
+    ptr = 1 << 20   # never dereferenced: every case fails its checks first
+    ok_args = dict(Q=ptr, K=ptr, V=ptr, O=ptr, B=1, H=1, N=8, d=64, M=8.0, pos0=0,
+                   dtype=binding.AAREN_BF16, S_in=None, z_in=None, S_out=None, z_out=None)
+
+    def call(**kw):
+        a = dict(ok_args, **kw)
+        return f(a["Q"], a["K"], a["V"], a["O"], a["B"], a["H"], a["N"], a["d"], a["M"],
+                 a["pos0"], a["dtype"], a["S_in"], a["z_in"], a["S_out"], a["z_out"], None)
+
+    assert call(d=32) == binding.AAREN_ERR_UNSUPPORTED
+    assert call(d=128) == binding.AAREN_ERR_UNSUPPORTED
+    assert call(dtype=binding.AAREN_F32) == binding.AAREN_ERR_UNSUPPORTED
+    assert call(M=0.0) == binding.AAREN_ERR_INVALID
+    assert call(M=-3.0) == binding.AAREN_ERR_INVALID
+    assert call(M=float("inf")) == binding.AAREN_ERR_INVALID
+    assert call(M=float("nan")) == binding.AAREN_ERR_INVALID
+    assert call(pos0=-1) == binding.AAREN_ERR_INVALID
+    assert call(N=-1) == binding.AAREN_ERR_INVALID
+    assert call(S_in=ptr) == binding.AAREN_ERR_INVALID          # z_in missing
+    assert call(S_out=ptr) == binding.AAREN_ERR_INVALID         # z_out missing
+    assert call(S_in=ptr + 4, z_in=ptr) == binding.AAREN_ERR_INVALID   # misaligned state
+    assert call(Q=None) == binding.AAREN_ERR_INVALID
+    assert call(O=ptr + 8) == binding.AAREN_ERR_INVALID          # misaligned output
+    assert call(B=0) == binding.AAREN_OK                         # nothing to do
+    assert call(N=1 << 31) == binding.AAREN_ERR_INVALID          # beyond the 32-bit coordinates
