@@ -32,15 +32,17 @@
 // chunk by chunk (g counts this CTA's chunks).  Roles:
 //   warp 0, one thread   tiled TMA loads of Q, K, V (two stages)
 //   warp 1, one thread   issues the MMAs as their operands become ready
-//   warpgroup 1 (warps 4-7, thread = token row i = TMEM lane): ReLU of Q in
-//       place; P -> A (causal mask, cos weight, hi/lo) back into tensor
-//       memory; o_i from intra, inter and the denominators.  The ReLU of the
-//       next chunk's Q runs while MMA2 of this chunk executes.
-//   warpgroup 2 (warps 8-11): as token rows, ReLU of K in place and the
-//       weighted keys as hi/lo; as state rows (r < 64 cos part, key dim r;
-//       r >= 64 sin part) its S row (64 floats) and z entry in registers,
-//       dS and dz added after each chunk, S and z published as hi/lo for the
-//       next chunk's MMA3, the final state written at the end of a head.
+//   two row warpgroups (warps 4-7 and 8-11, thread = token row i = TMEM
+//       lane; warpgroup hf takes columns 64hf.. of P and dims 32hf.. of O):
+//       ReLU of Q and K in place (half of each row each); P -> A (causal
+//       mask, cos weight, hi/lo) back into tensor memory, skipping blocks the
+//       mask zeroes; o_i from intra, inter and the denominators.  The ReLU of
+//       the next chunk runs while MMA2 of this chunk executes.
+//   key / state warpgroup (warps 12-15): as token rows, the weighted keys as
+//       hi/lo; as state rows (r < 64 cos part, key dim r; r >= 64 sin part)
+//       its S row (64 floats) and z entry in registers, dS and dz added after
+//       each chunk, S and z published as hi/lo for the next chunk's MMA3, the
+//       final state written at the end of a head.
 #pragma once
 
 #include <cuda.h>
@@ -57,7 +59,7 @@ namespace la {
 constexpr int C = 128;                     // tokens per chunk
 constexpr int D = 64;                      // head dimension (one 128-byte row)
 constexpr int kTile = C * D * 2;           // 16 KB: one [128 x 64] bf16 tile
-constexpr int kThreads = 384;
+constexpr int kThreads = 512;
 constexpr uint32_t kTmemCols = 512;
 
 // Shared-memory map (offsets from a 1024-byte aligned base).
@@ -92,13 +94,13 @@ struct Params {
 };
 
 struct Bars {
-    uint64_t full[2], empty[2];   // TMA stages
-    uint64_t qk;                  // ReLU of Q (warpgroup 1) and K (warpgroup 2) done: MMA1
+    uint64_t full[2], empty[2];   // TMA stages (empty: both row warpgroups and the key warpgroup)
+    uint64_t qk[2];               // per stage: ReLU of Q and K done (both row warpgroups): MMA1
     uint64_t kw;                  // weighted keys written: MMA4
     uint64_t sready;              // S, z published: MMA3
-    uint64_t aready;              // A in tensor memory: MMA2
+    uint64_t aready;              // A in tensor memory (both row warpgroups): MMA2
     uint64_t pfull, dsfull, ofull;   // MMA completion (commit)
-    uint64_t tfree;               // inter / intra read by warpgroup 1
+    uint64_t tfree;               // inter / intra read (both row warpgroups)
     uint32_t tmem;
     int abort;
 };
@@ -118,12 +120,14 @@ __device__ __forceinline__ uint32_t bf2_bits(float a, float b)
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-// (a, b) -> hi = bf16x2(a, b), lo = bf16x2(a - hi.a, b - hi.b): x = hi + lo
-// to about 2^-17 relative.
+// (a, b) -> hi = the bfloat16 truncations of a and b (their top 16 bits),
+// lo = bf16x2(a - hi.a, b - hi.b) rounded to nearest: x = hi + lo to within
+// 2^-16 relative (the remainder is below 2^-7 |x| and keeps 8 bits).
 __device__ __forceinline__ void split2(float a, float b, uint32_t &hi, uint32_t &lo)
 {
-    hi = bf2_bits(a, b);
-    lo = bf2_bits(a - bf_lo(hi), b - bf_hi(hi));
+    const uint32_t ua = __float_as_uint(a), ub = __float_as_uint(b);
+    hi = __byte_perm(ua, ub, 0x7632);
+    lo = bf2_bits(a - __uint_as_float(ua & 0xFFFF0000u), b - __uint_as_float(ub & 0xFFFF0000u));
 }
 
 __device__ __forceinline__ bool aborted(const Bars &b) { return *reinterpret_cast<const volatile int *>(&b.abort) != 0; }
@@ -175,14 +179,18 @@ __device__ __forceinline__ void pos_angle(int64_t pos, double inv_2M, float &cs,
     sincospif(static_cast<float>(static_cast<double>(pos) * inv_2M), &sn, &cs);
 }
 
-// ReLU of one 128-byte row in place.
-__device__ __forceinline__ void relu_row(uint8_t *row)
+// ReLU of half of one 128-byte row (row index r, half hf: slots visited 4hf
+// .. 4hf+3) in place.  The 16-byte slots are visited in the order slot = ch ^
+// (r % 8), so the eight rows a quarter-warp touches at a time sit in eight
+// different bank groups.
+__device__ __forceinline__ void relu_half_row(uint8_t *row, int r, int hf)
 {
 #pragma unroll
-    for (int ch = 0; ch < 8; ++ch) {
-        uint4 x = reinterpret_cast<uint4 *>(row)[ch];
+    for (int ch = 4 * hf; ch < 4 * hf + 4; ++ch) {
+        uint4 *slot = reinterpret_cast<uint4 *>(row) + (ch ^ (r & 7));
+        uint4 x = *slot;
         x.x = relu_bf16x2(x.x); x.y = relu_bf16x2(x.y); x.z = relu_bf16x2(x.z); x.w = relu_bf16x2(x.w);
-        reinterpret_cast<uint4 *>(row)[ch] = x;
+        *slot = x;
     }
 }
 
@@ -202,10 +210,11 @@ k_linattn(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtens
 
     if (tid == 0) {
         ptx::mbar_init(&b.full[0], 1); ptx::mbar_init(&b.full[1], 1);
-        ptx::mbar_init(&b.empty[0], 2); ptx::mbar_init(&b.empty[1], 2);
-        ptx::mbar_init(&b.qk, 2); ptx::mbar_init(&b.kw, 1); ptx::mbar_init(&b.sready, 1);
-        ptx::mbar_init(&b.aready, 1); ptx::mbar_init(&b.pfull, 1); ptx::mbar_init(&b.dsfull, 1);
-        ptx::mbar_init(&b.ofull, 1); ptx::mbar_init(&b.tfree, 1);
+        ptx::mbar_init(&b.empty[0], 3); ptx::mbar_init(&b.empty[1], 3);
+        ptx::mbar_init(&b.qk[0], 2); ptx::mbar_init(&b.qk[1], 2);
+        ptx::mbar_init(&b.kw, 1); ptx::mbar_init(&b.sready, 1); ptx::mbar_init(&b.aready, 2);
+        ptx::mbar_init(&b.pfull, 1); ptx::mbar_init(&b.dsfull, 1); ptx::mbar_init(&b.ofull, 1);
+        ptx::mbar_init(&b.tfree, 2);
         b.abort = 0;
         ptx::fence_barrier_init();
     }
@@ -221,7 +230,7 @@ k_linattn(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtens
         reinterpret_cast<uint4 *>(sm + OFF_S + kSPart + 2 * 8192)[x] = make_uint4(0u, 0u, 0u, 0u);
     }
     if (tid < 256) {
-        float* Ww = reinterpret_cast<float *>(sm + OFF_W);
+        float *Ww = reinterpret_cast<float *>(sm + OFF_W);
         Ww[tid] = tid >= C ? static_cast<float>(cospi(static_cast<double>(tid - C) * p.inv_2M)) : 0.f;
     }
     tc::fence_async_smem();
@@ -261,7 +270,7 @@ k_linattn(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtens
                 const unsigned par = static_cast<unsigned>(g & 1), prev = par ^ 1u;
                 const uint32_t q0 = tc::saddr(sm + OFF_STAGE + s * 3 * kTile);
                 const uint32_t k0 = q0 + kTile, v0 = q0 + 2 * kTile;
-                la_wait(b, &b.qk, par, p);
+                la_wait(b, &b.qk[s], static_cast<unsigned>((g >> 1) & 1), p);
                 if (g > 0) la_wait(b, &b.ofull, prev, p);   // MMA2 of the previous chunk has read A
                 if (aborted(b)) break;
                 tc::fence_after();
@@ -307,88 +316,103 @@ k_linattn(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtens
             if (aborted(b) && last != nullptr)   // gave up: let MMAs still in flight finish
                 wait_bar(last, last_par, p.wait_limit_ns);
         }
-    } else if (warp >= 4 && warp < 8) {
-        // ---------------- warpgroup 1: token rows ----------------
-        const int i = tid - 128;                                  // token row = TMEM lane
+    } else if (warp >= 4 && warp < 12) {
+        // ---------------- row warpgroups: token rows, half hf of the columns each ----------------
+        const int hf = (warp - 4) >> 2;                           // 0: warps 4-7, 1: warps 8-11
+        const unsigned nb = 1 + hf;                               // named barrier of this warpgroup
+        const int i = (warp & 3) * 32 + lane;                     // token row = TMEM lane
+        const bool leader = (warp & 3) == 0 && lane == 0;
         const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
         if (total > 0) {
             la_wait(b, &b.full[0], 0, p);
-            relu_row(sm + OFF_STAGE + i * 128);
+            relu_half_row(sm + OFF_STAGE + i * 128, i, hf);
+            relu_half_row(sm + OFF_STAGE + kTile + i * 128, i, hf);
             tc::fence_async_smem();
-            ptx::named_bar_sync(1, 128);
-            if (i == 0) ptx::mbar_arrive(&b.qk);
+            ptx::named_bar_sync(nb, 128);
+            if (leader) ptx::mbar_arrive(&b.qk[0]);
         }
         for (int64_t g = 0; g < total; ++g) {
-            if (stop_all(1, aborted(b))) break;
+            if (stop_all(nb, aborted(b))) break;
             const int s = static_cast<int>(g & 1);
             const unsigned par = static_cast<unsigned>(g & 1);
             const int64_t h = blockIdx.x + (g / nc) * gridDim.x, c = g % nc;
             float cs, sn;
             pos_angle(p.pos0 + c * C + i + 1, p.inv_2M, cs, sn);
 
-            // ---- P -> A: causal mask and cos weight (table), hi/lo pairs ----
+            // ---- P -> A on columns 64 hf .. 64 hf + 63: causal mask and cos weight, hi/lo ----
             la_wait(b, &b.pfull, par, p);
             tc::fence_after();
             __syncwarp();
-            const float *wrow = Wt + C + i;   // wrow[-j] = weight of column j
+            const float *wrow = Wt + C + i;   // wrow[-j] = weight of column j (0 for j > i)
 #pragma unroll 1
-            for (int qb = 0; qb < 4; ++qb) {
-                float pv[32];
-                tc::ld32(tmem + lane_base + COL_P + 32 * qb, pv);
+            for (int qb = 2 * hf; qb < 2 * hf + 2; ++qb) {
                 uint32_t wv[32];
+                if (qb > (warp & 3)) {         // every row of this warp is above the block: A = 0
 #pragma unroll
-                for (int t = 0; t < 32; t += 2) {
-                    const int j = 32 * qb + t;
-                    split2(pv[t] * wrow[-j], pv[t + 1] * wrow[-j - 1], wv[t >> 1], wv[16 + (t >> 1)]);
+                    for (int t = 0; t < 32; ++t) wv[t] = 0u;
+                } else {
+                    uint32_t pc[32];
+                    tc::ld32_async(tmem + lane_base + COL_P + 32 * qb, pc);
+                    tc::wait_ld();
+#pragma unroll
+                    for (int t = 0; t < 32; t += 2) {
+                        const int j = 32 * qb + t;
+                        split2(__uint_as_float(pc[t]) * wrow[-j], __uint_as_float(pc[t + 1]) * wrow[-j - 1],
+                               wv[t >> 1], wv[16 + (t >> 1)]);
+                    }
                 }
                 tc::st32(tmem + lane_base + COL_P + 32 * qb, wv);
             }
             tc::wait_st();
             tc::fence_before();
-            ptx::named_bar_sync(1, 128);
-            if (i == 0) ptx::mbar_arrive(&b.aready);
+            ptx::named_bar_sync(nb, 128);
+            if (leader) ptx::mbar_arrive(&b.aready);
 
-            // ---- ReLU of the next chunk's Q while MMA2 runs ----
+            // ---- ReLU of the next chunk's Q and K (this half of each row) while MMA2 runs ----
             if (g + 1 < total) {
                 const int s1 = static_cast<int>((g + 1) & 1);
                 la_wait(b, &b.full[s1], static_cast<unsigned>(((g + 1) >> 1) & 1), p);
-                relu_row(sm + OFF_STAGE + s1 * 3 * kTile + i * 128);
+                uint8_t *st1 = sm + OFF_STAGE + s1 * 3 * kTile;
+                relu_half_row(st1 + i * 128, i, hf);
+                relu_half_row(st1 + kTile + i * 128, i, hf);
                 tc::fence_async_smem();
-                ptx::named_bar_sync(1, 128);
-                if (i == 0) ptx::mbar_arrive(&b.qk);
+                ptx::named_bar_sync(nb, 128);
+                if (leader) ptx::mbar_arrive(&b.qk[s1]);
             }
 
-            // ---- o_i = (intra + cos inter_c + sin inter_s) / (den_intra + cos Q'.z^c + sin Q'.z^s) ----
+            // ---- o_i on dims 32 hf .. 32 hf + 31:
+            //      (intra + cos inter_c + sin inter_s) / (den_intra + cos Q'.z^c + sin Q'.z^s) ----
             la_wait(b, &b.ofull, par, p);
             tc::fence_after();
             __syncwarp();
-            float dx, dx1, qzc, qzs;
-            tc::ld2(tmem + lane_base + COL_X + 64, dx, dx1);
-            tc::ld2(tmem + lane_base + COL_I + 128, qzc, qzs);
-            const float dt = dx + cs * qzc + sn * qzs;
-            const float r = dt != 0.f ? 1.f / dt : 0.f;
-            const int64_t row = c * C + i;
-            Tout *orow = reinterpret_cast<Tout *>(p.O) + (h * p.N + row) * D;
-#pragma unroll 1
-            for (int b0 = 0; b0 < 64; b0 += 32) {
-                float x[32], ic[32], is[32];
-                tc::ld32(tmem + lane_base + COL_X + b0, x);
-                tc::ld32(tmem + lane_base + COL_I + b0, ic);
-                tc::ld32(tmem + lane_base + COL_I + 64 + b0, is);
+            {
+                const int b0 = 32 * hf;
+                uint32_t x[32], ic[32], is[32], d0, d1, z0, z1;
+                tc::ld32_async(tmem + lane_base + COL_X + b0, x);
+                tc::ld32_async(tmem + lane_base + COL_I + b0, ic);
+                tc::ld32_async(tmem + lane_base + COL_I + 64 + b0, is);
+                tc::ld2_async(tmem + lane_base + COL_X + 64, d0, d1);
+                tc::ld2_async(tmem + lane_base + COL_I + 128, z0, z1);
+                tc::wait_ld();
+                const float dt = __uint_as_float(d0) + cs * __uint_as_float(z0) + sn * __uint_as_float(z1);
+                const float r = dt != 0.f ? 1.f / dt : 0.f;
+                float o[32];
 #pragma unroll
-                for (int t = 0; t < 32; ++t) x[t] = (x[t] + cs * ic[t] + sn * is[t]) * r;
-                if (row < p.N) store_row32(orow + b0, x);
+                for (int t = 0; t < 32; ++t)
+                    o[t] = (__uint_as_float(x[t]) + cs * __uint_as_float(ic[t]) + sn * __uint_as_float(is[t])) * r;
+                const int64_t row = c * C + i;
+                if (row < p.N) store_row32(reinterpret_cast<Tout *>(p.O) + (h * p.N + row) * D + b0, o);
             }
             tc::fence_before();
-            ptx::named_bar_sync(1, 128);
-            if (i == 0) {
+            ptx::named_bar_sync(nb, 128);
+            if (leader) {
                 ptx::mbar_arrive(&b.tfree);
                 ptx::mbar_arrive(&b.empty[s]);
             }
         }
-    } else if (warp >= 8) {
-        // ---------------- warpgroup 2: keys and state ----------------
-        const int r = tid - 256;                 // token row (key work) and state row (dS lane)
+    } else if (warp >= 12) {
+        // ---------------- key / state warpgroup ----------------
+        const int r = tid - 384;                 // token row (key work) and state row (dS lane)
         const int half = r >> 6, k = r & 63;
         const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
         uint8_t *kw = sm + OFF_KW;
@@ -397,7 +421,7 @@ k_linattn(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtens
         float S[64];
         float z = 0.f;
         for (int64_t g = 0; g < total; ++g) {
-            if (stop_all(2, aborted(b))) break;
+            if (stop_all(3, aborted(b))) break;
             const int s = static_cast<int>(g & 1);
             const unsigned par = static_cast<unsigned>(g & 1);
             const int64_t h = blockIdx.x + (g / nc) * gridDim.x, c = g % nc;
@@ -417,20 +441,16 @@ k_linattn(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtens
                 }
             }
 
-            // ---- keys: ReLU in place (MMA1), then cos / sin weighted as hi/lo (MMA4) ----
-            la_wait(b, &b.full[s], static_cast<unsigned>((g >> 1) & 1), p);
-            const uint8_t *krow = sm + OFF_STAGE + s * 3 * kTile + kTile + r * 128;
-            relu_row(const_cast<uint8_t *>(krow));
-            tc::fence_async_smem();
-            tc::fence_before();
-            ptx::named_bar_sync(2, 128);
-            if (r == 0) ptx::mbar_arrive(&b.qk);
+            // ---- keys (ReLU'd by the row warpgroups): cos / sin weighted as hi/lo (MMA4) ----
+            la_wait(b, &b.qk[s], static_cast<unsigned>((g >> 1) & 1), p);
             {
+                const uint8_t *krow = sm + OFF_STAGE + s * 3 * kTile + kTile + r * 128;
                 float cs, sn;
                 pos_angle(p.pos0 + c * C + r + 1, p.inv_2M, cs, sn);
 #pragma unroll
                 for (int ch = 0; ch < 8; ++ch) {
-                    const uint4 kx = reinterpret_cast<const uint4 *>(krow)[ch];   // this thread's own row
+                    const int slot = ch ^ (r & 7);   // conflict-free order, as in relu_half_row
+                    const uint4 kx = reinterpret_cast<const uint4 *>(krow)[slot];
                     const uint32_t w4[4] = {kx.x, kx.y, kx.z, kx.w};
                     uint32_t hc[4], lc[4], hs[4], ls[4];
 #pragma unroll
@@ -439,7 +459,7 @@ k_linattn(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtens
                         split2(x0 * cs, x1 * cs, hc[e], lc[e]);
                         split2(x0 * sn, x1 * sn, hs[e], ls[e]);
                     }
-                    const int off = r * 128 + ch * 16;   // same physical slot: same swizzle
+                    const int off = r * 128 + slot * 16;   // same physical slot: same swizzle
                     *reinterpret_cast<uint4 *>(kw + 0 * kTile + off) = make_uint4(hc[0], hc[1], hc[2], hc[3]);
                     *reinterpret_cast<uint4 *>(kw + 1 * kTile + off) = make_uint4(hs[0], hs[1], hs[2], hs[3]);
                     *reinterpret_cast<uint4 *>(kw + 2 * kTile + off) = make_uint4(lc[0], lc[1], lc[2], lc[3]);
@@ -447,7 +467,8 @@ k_linattn(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtens
                 }
             }
             tc::fence_async_smem();
-            ptx::named_bar_sync(2, 128);
+            tc::fence_before();
+            ptx::named_bar_sync(3, 128);
             if (r == 0) {
                 ptx::mbar_arrive(&b.kw);
                 ptx::mbar_arrive(&b.empty[s]);
@@ -473,7 +494,7 @@ k_linattn(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtens
             }
             tc::fence_async_smem();
             tc::fence_before();
-            ptx::named_bar_sync(2, 128);
+            ptx::named_bar_sync(3, 128);
             if (r == 0) ptx::mbar_arrive(&b.sready);
 
             // ---- dS, dz of this chunk ----

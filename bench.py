@@ -58,11 +58,12 @@ def parse():
     ap.add_argument("--heads", type=int, default=0, help="override H (profiling small cases)")
     ap.add_argument("--tokens", type=int, default=0, help="override N (profiling small cases)")
     ap.add_argument("--out-dtype", default="", choices=["", "bf16", "f32"])
-    ap.add_argument("--op", default="scan", choices=["scan", "reduce", "backward", "step"],
+    ap.add_argument("--op", default="scan", choices=["scan", "reduce", "backward", "step", "linattn"],
                     help="scan: every prefix output (the headline); reduce: the many-to-one "
                          "form (o_N and the final state only); backward: dq, dK, dV of the "
                          "scan from O, dO and the saved per-prefix statistics; step: the "
-                         "one-token update of many streams (the stream workload)")
+                         "one-token update of many streams (the stream workload); linattn: "
+                         "the causal cos-re-weighted linear attention (the linattn workload)")
     return ap.parse_args()
 
 
@@ -575,8 +576,195 @@ def run_step(args):
     return 0
 
 
+LA_CPU_TOKENS = 512        # oracle sample: leading tokens of each sampled head
+LA_CPU_HEADS = 64
+
+
+def la_cpu_rate(wl, tokens, heads, threads, min_s=0.0):
+    """Time the float64 linear-attention oracle (as it stands) on the first
+    `tokens` tokens of the first `heads` heads, spread over `threads` host
+    threads, repeated until `min_s` seconds have elapsed.  Returns
+    (head-tokens/s, seconds, tokens, heads, passes)."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    import oracle
+    from attention_prefix_scan_02_b300 import inputs
+    n = min(tokens, wl.N)
+    sub_wl = inputs.custom(wl.B, wl.H, n, wl.d, wl.dtype, wl.seed, wl.kind, wl.name)
+    hs = [(b, h) for b in range(wl.B) for h in range(wl.H)][:heads]
+    data = [inputs.head_token_inputs(sub_wl, b, h) for b, h in hs]
+
+    def one(x):
+        oracle.la_scan(*x, float(wl.N))
+
+    passes = 0
+    t0 = time.perf_counter()
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        while True:
+            list(ex.map(one, data))
+            passes += 1
+            dt = time.perf_counter() - t0
+            if dt >= min_s or passes >= CPU_SAMPLE_MAX_PASSES:
+                break
+    return passes * len(data) * n / dt, dt, n, len(data), passes
+
+
+def run_linattn(args):
+    """The causal cos-re-weighted linear attention on the linattn workload
+    (B=64, H=16, N=2048, d=64, bf16 in; one query per token): one
+    aaren_linattn_forward per step, inputs resident in HBM (1.07 GB of Q, K,
+    V, larger than L2).  Algorithmic bytes: Q, K, V read once and O written
+    once per head-token."""
+    import torch
+
+    rank, world, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (the library has no CPU path)")
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    from attention_prefix_scan_02_b300 import binding, build, inputs
+    build.build()
+    wl = inputs.WORKLOADS["linattn"]
+    out = args.out_dtype or wl.dtype
+    out_t = torch.bfloat16 if out == "bf16" else torch.float32
+    warmup = max(3, args.warmup)
+    cpu = None
+    if rank == 0:
+        threads = min(host_cores(), LA_CPU_HEADS)
+        rate, dt, n, nh, passes = la_cpu_rate(wl, LA_CPU_TOKENS, LA_CPU_HEADS, threads, CPU_SAMPLE_MIN_S)
+        cpu = {"value": rate, "unit": "head-tokens/s", "cores": threads, "kind": "oracle",
+               "sample": f"the first {n} tokens of {nh} heads ({n * nh} head-tokens), {passes} passes, "
+                         f"{dt:.1f} s wall on {threads} threads"}
+    Q, K, V = inputs.token_inputs(wl, device="cuda", b0=rank * wl.B)
+    O = torch.empty(K.shape, dtype=out_t, device="cuda")
+    stream = torch.cuda.current_stream()
+    M = float(wl.N)
+
+    def call(Q, K, V, O):
+        binding.aaren_linattn_forward(Q, K, V, O, M, stream=stream)
+
+    for _ in range(warmup):
+        call(Q, K, V, O)
+    if binding.aaren_check() != binding.AAREN_OK:
+        raise SystemExit("device status error during warm-up")
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        time.sleep(0.3)
+        clocks.begin = time.time()
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        for i in range(args.steps):
+            starts[i].record(stream)
+            call(Q, K, V, O)
+            ends[i].record(stream)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+        clocks.end = time.time()
+    if dist is not None:
+        dist.barrier()
+    status = binding.aaren_check()
+    if status != binding.AAREN_OK:
+        raise SystemExit(f"device status error in the timed region: {binding.status_string(status)}")
+    mean_launch_ms = statistics.mean(s.elapsed_time(e) for s, e in zip(starts, ends))
+    step_ms = max_over_ranks(t_start.elapsed_time(t_end) / args.steps, dist, "cuda")
+    tokens = wl.heads * wl.N
+    elems = tokens * wl.d
+    out_b = 2 if out == "bf16" else 4
+    alg_bytes = elems * (3 * 2 + out_b)
+
+    # end to end with pinned host buffers: Q, K, V in and O out inside the timed region
+    hQ, hK, hV = (torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (Q, K, V))
+    hO = torch.empty(O.shape, dtype=out_t, pin_memory=True)
+    hQ.copy_(Q); hK.copy_(K); hV.copy_(V)
+    e2e_steps = max(1, min(args.steps, 3))
+
+    def e2e_step():
+        Q.copy_(hQ, non_blocking=True); K.copy_(hK, non_blocking=True); V.copy_(hV, non_blocking=True)
+        call(Q, K, V, O)
+        hO.copy_(O, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True); b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(a.elapsed_time(b) / e2e_steps, dist, "cuda")
+    if binding.aaren_check() != binding.AAREN_OK:
+        raise SystemExit("device status error in the end-to-end leg")
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return 0
+    peak, peak_src = measured_peak()
+    achieved = alg_bytes / (mean_launch_ms * 1e-3) / 1e9
+    line = {
+        "metric": METRIC + " (causal cos-re-weighted linear attention)",
+        "value": whole_job_rate(tokens, world, step_ms), "unit": "head-tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": warmup, "ms_per_step": step_ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": f"linattn: B={wl.B} H={wl.H} N={wl.N} d={wl.d}, bf16 in, {out} out, "
+                               f"Q, K, V ~ N(0,1) (a query per token), M = N, seed {wl.seed}",
+                   "op": "linattn", "global_batch": world * wl.B,
+                   "parallelism": f"independent sequences, {world} rank(s), no collective",
+                   "l2": "no flush: Q, K, V per step (1.07 GB) far larger than the 126 MB L2"},
+        "gpu_launches": args.steps,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": None,
+                     "algorithmic_bytes_per_launch": alg_bytes, "launch_ms": mean_launch_ms,
+                     "peak_source": peak_src, "kernel": "k_linattn"},
+        "cpu_baseline": cpu,
+        "e2e": {"value": whole_job_rate(tokens, world, e2e_ms), "unit": "head-tokens/s",
+                "h2d_bytes_per_step": 3 * elems * 2, "d2h_bytes_per_step": elems * out_b,
+                "ms_per_step": e2e_ms, "steps": e2e_steps,
+                "path": "pinned host Q,K,V -> device, aaren_linattn_forward, device O -> pinned host"},
+        "clocks": clocks.summary(),
+    }
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
 def main():
     args = parse()
+    if args.impl == "reference" and args.op == "linattn":
+        rank, _, _ = dist_env()
+        if rank != 0:
+            return 0
+        from attention_prefix_scan_02_b300 import inputs
+        wl = inputs.WORKLOADS["linattn"]
+        threads = min(host_cores(), LA_CPU_HEADS)
+        rates = []
+        for i in range(args.warmup + args.steps):
+            r, dt, n, nh, _ = la_cpu_rate(wl, LA_CPU_TOKENS, LA_CPU_HEADS, threads)
+            if i >= args.warmup:
+                rates.append((r, dt))
+        value = statistics.mean(r for r, _ in rates)
+        print(json.dumps({"impl": "reference", "metric": METRIC + " (causal cos-re-weighted linear attention)",
+                          "value": value, "unit": "head-tokens/s", "n_gpus": args.gpus, "steps": args.steps,
+                          "warmup": args.warmup, "ms_per_step": 1e3 * statistics.mean(dt for _, dt in rates),
+                          "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                          "data": "synthetic", "config": {"workload": "linattn", "op": "linattn"},
+                          "cpu_baseline": {"value": value, "unit": "head-tokens/s", "cores": threads,
+                                           "kind": "oracle",
+                                           "sample": f"each step: the first {n} tokens of {nh} heads"},
+                          "e2e": {"value": value, "unit": "head-tokens/s", "h2d_bytes_per_step": 0,
+                                  "d2h_bytes_per_step": 0}}), flush=True)
+        return 0
+    if args.op == "linattn":
+        return run_linattn(args)
     if args.impl == "reference":
         return run_reference(args)
     if args.op == "step":
