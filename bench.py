@@ -113,28 +113,35 @@ def describe(wl, out):
             else "L2 flushed (write of 2x L2 size) before every timed step"}
 
 
-def kernel_source_hash():
+# the source files each profiled kernel is built from (its own code and what it includes)
+KERNEL_SOURCES = {
+    "k_scan_pipe": ["scan_pipe_kernel.cuh", "scan_kernel.cuh", "common.cuh", "ptx.cuh"],
+    "k_linattn": ["linattn_kernel.cuh", "tc.cuh", "scan_kernel.cuh", "common.cuh", "ptx.cuh"],
+}
+
+
+def kernel_source_hash(kernel):
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "attention_prefix_scan_02_b300", "csrc")
-    for fn in sorted(os.listdir(csrc)):
+    for fn in sorted(KERNEL_SOURCES[kernel]):
         with open(os.path.join(csrc, fn), "rb") as f:
             h.update(fn.encode() + f.read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(wl, out):
+def profiled_traffic(wl, out, record="scan_long_bf16_traffic.json", kernel="k_scan_pipe"):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel source with this head size, dtype and output type;
-    else None.  The capture is of a shorter sequence (the full launch is too
-    large for a multi-pass capture); its bytes per head-token are scaled to
-    this launch's head-tokens."""
-    path = os.path.join(ROOT, "profiles", "scan_long_bf16_traffic.json")
+    on the current source of the kernel with this head size, dtype and output
+    type; else None.  The capture is of a smaller case (the full launch is
+    too large for a multi-pass capture); its bytes per head-token are scaled
+    to this launch's head-tokens."""
+    path = os.path.join(ROOT, "profiles", record)
     try:
         with open(path) as f:
             rec = json.load(f)
     except (OSError, ValueError):
         return None
-    if rec.get("kernel_source_sha") != kernel_source_hash():
+    if rec.get("kernel_source_sha") != kernel_source_hash(kernel):
         return None
     if (rec.get("d") != wl.d or rec.get("in_dtype") != wl.dtype or rec.get("out_dtype") != out):
         return None
@@ -721,7 +728,8 @@ def run_linattn(args):
                    "l2": "no flush: Q, K, V per step (1.07 GB) far larger than the 126 MB L2"},
         "gpu_launches": args.steps,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": None,
+                     "frac": achieved / peak,
+                     "traffic": profiled_traffic(wl, out, "linattn_bf16_traffic.json", "k_linattn"),
                      "algorithmic_bytes_per_launch": alg_bytes, "launch_ms": mean_launch_ms,
                      "peak_source": peak_src, "kernel": "k_linattn"},
         "cpu_baseline": cpu,
