@@ -548,10 +548,14 @@ __global__ void __launch_bounds__(PipeTile<D, GROUPS, STAGES>::THREADS, 1)
             __syncwarp();
         }
 
-        // 3. warp 0 publishes the chunk aggregate for successors' look-backs
-        //    (its wait for the carry would otherwise be idle); the carry warp
-        //    may already have published the inclusive prefix, which wins
-        if (wg == 0 && c > 0) {
+        // 3. compute warp 1 publishes the chunk aggregate for successors'
+        //    look-backs as soon as the four warp aggregates exist (warp 0 is
+        //    busy handing the stage back; the wait for the carry would
+        //    otherwise be idle).  A successor's look-back waits for the
+        //    aggregates of every predecessor still in flight, so this
+        //    publication sets the pace of the whole scan.  The carry warp
+        //    may already have published the inclusive prefix, which wins.
+        if (wg == (kPipeComputeWarps > 1 ? 1 : 0) && c > 0) {
             const int64_t chunk = head * p.chunks_per_head + c;
             if (chunk != p.fault_chunk && compute_wait(aggb, par, group_limit)) {
                 float am, aw, au[E];
