@@ -120,14 +120,40 @@ __device__ __forceinline__ uint32_t bf2_bits(float a, float b)
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-// (a, b) -> hi = the bfloat16 truncations of a and b (their top 16 bits),
-// lo = bf16x2(a - hi.a, b - hi.b) rounded to nearest: x = hi + lo to within
-// 2^-16 relative (the remainder is below 2^-7 |x| and keeps 8 bits).
+// Packed float32 pairs (sm_100 family f32x2 arithmetic): .x in the low word.
+__device__ __forceinline__ uint64_t f2(float a, float b)
+{
+    return static_cast<uint64_t>(__float_as_uint(a)) | (static_cast<uint64_t>(__float_as_uint(b)) << 32);
+}
+
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b)
+{
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+__device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b)
+{
+    uint64_t d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+// pair (a, b) -> hi = the bfloat16 truncations of a and b (their top 16
+// bits), lo = bf16x2(a - hi.a, b - hi.b) rounded to nearest: x = hi + lo to
+// within 2^-16 relative (the remainder is below 2^-7 |x| and keeps 8 bits).
+__device__ __forceinline__ void split2p(uint64_t ab, uint32_t &hi, uint32_t &lo)
+{
+    const uint32_t ua = static_cast<uint32_t>(ab), ub = static_cast<uint32_t>(ab >> 32);
+    hi = __byte_perm(ua, ub, 0x7632);
+    const uint64_t r = sub2(ab, (ab & 0xFFFF0000FFFF0000ull));
+    lo = bf2_bits(__uint_as_float(static_cast<uint32_t>(r)), __uint_as_float(static_cast<uint32_t>(r >> 32)));
+}
+
 __device__ __forceinline__ void split2(float a, float b, uint32_t &hi, uint32_t &lo)
 {
-    const uint32_t ua = __float_as_uint(a), ub = __float_as_uint(b);
-    hi = __byte_perm(ua, ub, 0x7632);
-    lo = bf2_bits(a - __uint_as_float(ua & 0xFFFF0000u), b - __uint_as_float(ub & 0xFFFF0000u));
+    split2p(f2(a, b), hi, lo);
 }
 
 __device__ __forceinline__ bool aborted(const Bars &b) { return *reinterpret_cast<const volatile int *>(&b.abort) != 0; }
@@ -357,8 +383,8 @@ k_linattn(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtens
 #pragma unroll
                     for (int t = 0; t < 32; t += 2) {
                         const int j = 32 * qb + t;
-                        split2(__uint_as_float(pc[t]) * wrow[-j], __uint_as_float(pc[t + 1]) * wrow[-j - 1],
-                               wv[t >> 1], wv[16 + (t >> 1)]);
+                        const uint64_t pp = static_cast<uint64_t>(pc[t]) | (static_cast<uint64_t>(pc[t + 1]) << 32);
+                        split2p(mul2(pp, f2(wrow[-j], wrow[-j - 1])), wv[t >> 1], wv[16 + (t >> 1)]);
                     }
                 }
                 tc::st32(tmem + lane_base + COL_P + 32 * qb, wv);
@@ -447,6 +473,7 @@ k_linattn(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtens
                 const uint8_t *krow = sm + OFF_STAGE + s * 3 * kTile + kTile + r * 128;
                 float cs, sn;
                 pos_angle(p.pos0 + c * C + r + 1, p.inv_2M, cs, sn);
+                const uint64_t c2 = f2(cs, cs), s2 = f2(sn, sn);
 #pragma unroll
                 for (int ch = 0; ch < 8; ++ch) {
                     const int slot = ch ^ (r & 7);   // conflict-free order, as in relu_half_row
@@ -455,9 +482,9 @@ k_linattn(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtens
                     uint32_t hc[4], lc[4], hs[4], ls[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const float x0 = bf_lo(w4[e]), x1 = bf_hi(w4[e]);
-                        split2(x0 * cs, x1 * cs, hc[e], lc[e]);
-                        split2(x0 * sn, x1 * sn, hs[e], ls[e]);
+                        const uint64_t x = f2(bf_lo(w4[e]), bf_hi(w4[e]));
+                        split2p(mul2(x, c2), hc[e], lc[e]);
+                        split2p(mul2(x, s2), hs[e], ls[e]);
                     }
                     const int off = r * 128 + slot * 16;   // same physical slot: same swizzle
                     *reinterpret_cast<uint4 *>(kw + 0 * kTile + off) = make_uint4(hc[0], hc[1], hc[2], hc[3]);
