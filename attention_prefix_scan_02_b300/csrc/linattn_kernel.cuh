@@ -306,38 +306,66 @@ k_linattn(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtens
                                ID_QK, kk > 0);
                 tc::commit(&b.pfull);
                 last = &b.pfull; last_par = par;
-                la_wait(b, &b.kw, par, p);
-                if (aborted(b)) break;
-                tc::fence_after();
+                // MMA4 (state update), MMA3 (inter) and MMA2 (intra) as their
+                // operands come ready, in whatever order that is; the output
+                // barrier covers MMA3 and MMA2, MMA4 has its own
+                bool d4 = false, d3 = false, d2 = false, dO = false, tf = (g == 0), timed_out = false;
+                const uint64_t t_start = ptx::globaltimer();
+                for (unsigned polls = 0; !(d4 && dO); ++polls) {
+                    bool any = false;
+                    if (!d4 && ptx::mbar_test_wait(&b.kw, par)) {
+                        tc::fence_after();
 #pragma unroll 1
-                for (int hl = 0; hl < 2; ++hl)
+                        for (int hl = 0; hl < 2; ++hl)
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)
-                        tc::mma_ss(tmem + COL_DS, tc::sdesc(kw0 + hl * 2 * kTile + kk * 2048, kTile, 1024),
-                                   tc::sdesc(v0 + kk * 2048, ones - v0, 1024), ID_KV, hl > 0 || kk > 0);
-                tc::commit(&b.dsfull);
-                last = &b.dsfull; last_par = par;
-                la_wait(b, &b.sready, par, p);
-                if (g > 0) la_wait(b, &b.tfree, prev, p);   // inter / intra of the previous chunk read
-                if (aborted(b)) break;
-                tc::fence_after();
+                            for (int kk = 0; kk < 8; ++kk)
+                                tc::mma_ss(tmem + COL_DS, tc::sdesc(kw0 + hl * 2 * kTile + kk * 2048, kTile, 1024),
+                                           tc::sdesc(v0 + kk * 2048, ones - v0, 1024), ID_KV, hl > 0 || kk > 0);
+                        tc::commit(&b.dsfull);
+                        last = &b.dsfull; last_par = par;
+                        d4 = any = true;
+                    }
+                    if (!tf) tf = ptx::mbar_test_wait(&b.tfree, prev);   // inter / intra of the previous chunk read
+                    if (tf && !d3 && ptx::mbar_test_wait(&b.sready, par)) {
+                        tc::fence_after();
 #pragma unroll 1
-                for (int hl = 0; hl < 2; ++hl)
+                        for (int hl = 0; hl < 2; ++hl)
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        tc::mma_ss(tmem + COL_I, tc::sdesc(q0 + kk * 32, 16, 1024),
-                                   tc::sdesc(s0 + hl * kSPart + kk * 2048, 8192, 1024), ID_QS, hl > 0 || kk > 0);
-                la_wait(b, &b.aready, par, p);
-                if (aborted(b)) break;
-                tc::fence_after();
+                            for (int kk = 0; kk < 4; ++kk)
+                                tc::mma_ss(tmem + COL_I, tc::sdesc(q0 + kk * 32, 16, 1024),
+                                           tc::sdesc(s0 + hl * kSPart + kk * 2048, 8192, 1024), ID_QS,
+                                           hl > 0 || kk > 0);
+                        d3 = any = true;
+                    }
+                    if (tf && !d2 && ptx::mbar_test_wait(&b.aready, par)) {
+                        tc::fence_after();
 #pragma unroll 1
-                for (int hl = 0; hl < 2; ++hl)
+                        for (int hl = 0; hl < 2; ++hl)
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)
-                        tc::mma_ts(tmem + COL_X, tmem + COL_P + 32 * (kk >> 1) + 16 * hl + 8 * (kk & 1),
-                                   tc::sdesc(v0 + kk * 2048, ones - v0, 1024), ID_AV, hl > 0 || kk > 0);
-                tc::commit(&b.ofull);
-                last = &b.ofull; last_par = par;
+                            for (int kk = 0; kk < 8; ++kk)
+                                tc::mma_ts(tmem + COL_X, tmem + COL_P + 32 * (kk >> 1) + 16 * hl + 8 * (kk & 1),
+                                           tc::sdesc(v0 + kk * 2048, ones - v0, 1024), ID_AV, hl > 0 || kk > 0);
+                        d2 = any = true;
+                    }
+                    if (d2 && d3 && !dO) {   // exactly one output commit per chunk
+                        tc::commit(&b.ofull);
+                        last = &b.ofull; last_par = par;
+                        dO = true;
+                    }
+                    if (!any) {
+                        if (aborted(b) ||
+                            (polls >= kMinWaitPolls && int64_t(ptx::globaltimer() - t_start) > p.wait_limit_ns)) {
+                            timed_out = true;
+                            break;
+                        }
+                        __nanosleep(32);
+                    }
+                }
+                if (timed_out) {
+                    atomicOr(p.status, STATUS_LOAD_TIMEOUT);
+                    *reinterpret_cast<volatile int *>(&b.abort) = 1;
+                    break;
+                }
             }
             if (aborted(b) && last != nullptr)   // gave up: let MMAs still in flight finish
                 wait_bar(last, last_par, p.wait_limit_ns);
@@ -446,28 +474,55 @@ k_linattn(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtens
         uint8_t *Zh = sm + OFF_S + 2 * 8192;      // z block, hi (column 0 = z^c, 1 = z^s)
         float S[64];
         float z = 0.f;
+        // the state a head starts from: the caller's, or zero
+        auto load_start = [&](int64_t h) {
+            if (p.S_in != nullptr) {
+                const float4 *src = reinterpret_cast<const float4 *>(p.S_in + ((h * 2 + half) * 64 + k) * 64);
+#pragma unroll
+                for (int q4 = 0; q4 < 16; ++q4) {
+                    const float4 v = src[q4];
+                    S[4 * q4] = v.x; S[4 * q4 + 1] = v.y; S[4 * q4 + 2] = v.z; S[4 * q4 + 3] = v.w;
+                }
+                z = p.z_in[(h * 2 + half) * 64 + k];
+            } else {
+#pragma unroll
+                for (int t = 0; t < 64; ++t) S[t] = 0.f;
+                z = 0.f;
+            }
+        };
+        // S and z of the next chunk's start as hi/lo (the B operand of MMA3)
+        auto publish_state = [&]() {
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch) {
+                uint32_t hw[4], lw[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) split2(S[8 * ch + 2 * e], S[8 * ch + 2 * e + 1], hw[e], lw[e]);
+                const int off = k * 128 + ((ch ^ (k & 7)) << 4);
+                *reinterpret_cast<uint4 *>(Sh + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                *reinterpret_cast<uint4 *>(Sh + kSPart + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+            }
+            const __nv_bfloat16 zh = __float2bfloat16_rn(z);
+            const __nv_bfloat16 zl = __float2bfloat16_rn(z - __bfloat162float(zh));
+            const int off = k * 128 + ((k & 7) << 4) + half * 2;   // row k, column half
+            *reinterpret_cast<__nv_bfloat16 *>(Zh + off) = zh;
+            *reinterpret_cast<__nv_bfloat16 *>(Zh + kSPart + off) = zl;
+            tc::fence_async_smem();
+            tc::fence_before();
+            ptx::named_bar_sync(3, 128);
+            if (r == 0) ptx::mbar_arrive(&b.sready);
+        };
+        if (total > 0) {
+            load_start(blockIdx.x);
+            publish_state();   // the first chunk's state
+        }
         for (int64_t g = 0; g < total; ++g) {
             if (stop_all(3, aborted(b))) break;
             const int s = static_cast<int>(g & 1);
             const unsigned par = static_cast<unsigned>(g & 1);
             const int64_t h = blockIdx.x + (g / nc) * gridDim.x, c = g % nc;
-            if (c == 0) {
-                if (p.S_in != nullptr) {
-                    const float4 *src = reinterpret_cast<const float4 *>(p.S_in + ((h * 2 + half) * 64 + k) * 64);
-#pragma unroll
-                    for (int q4 = 0; q4 < 16; ++q4) {
-                        const float4 v = src[q4];
-                        S[4 * q4] = v.x; S[4 * q4 + 1] = v.y; S[4 * q4 + 2] = v.z; S[4 * q4 + 3] = v.w;
-                    }
-                    z = p.z_in[(h * 2 + half) * 64 + k];
-                } else {
-#pragma unroll
-                    for (int t = 0; t < 64; ++t) S[t] = 0.f;
-                    z = 0.f;
-                }
-            }
 
-            // ---- keys (ReLU'd by the row warpgroups): cos / sin weighted as hi/lo (MMA4) ----
+            // ---- keys (ReLU'd by the row warpgroups): cos / sin weighted as hi/lo (MMA4);
+            //      the previous chunk's MMA4 is done with the buffer (dsfull waited below) ----
             la_wait(b, &b.qk[s], static_cast<unsigned>((g >> 1) & 1), p);
             {
                 const uint8_t *krow = sm + OFF_STAGE + s * 3 * kTile + kTile + r * 128;
@@ -496,35 +551,9 @@ k_linattn(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtens
             tc::fence_async_smem();
             tc::fence_before();
             ptx::named_bar_sync(3, 128);
-            if (r == 0) {
-                ptx::mbar_arrive(&b.kw);
-                ptx::mbar_arrive(&b.empty[s]);
-            }
+            if (r == 0) ptx::mbar_arrive(&b.kw);
 
-            // ---- publish S and z of this chunk's start as hi/lo (MMA3) ----
-            if (g > 0) la_wait(b, &b.ofull, par ^ 1u, p);   // MMA3 of the previous chunk has read them
-#pragma unroll
-            for (int ch = 0; ch < 8; ++ch) {
-                uint32_t hw[4], lw[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) split2(S[8 * ch + 2 * e], S[8 * ch + 2 * e + 1], hw[e], lw[e]);
-                const int off = k * 128 + ((ch ^ (k & 7)) << 4);
-                *reinterpret_cast<uint4 *>(Sh + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-                *reinterpret_cast<uint4 *>(Sh + kSPart + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-            }
-            {
-                const __nv_bfloat16 zh = __float2bfloat16_rn(z);
-                const __nv_bfloat16 zl = __float2bfloat16_rn(z - __bfloat162float(zh));
-                const int off = k * 128 + ((k & 7) << 4) + half * 2;   // row k, column half
-                *reinterpret_cast<__nv_bfloat16 *>(Zh + off) = zh;
-                *reinterpret_cast<__nv_bfloat16 *>(Zh + kSPart + off) = zl;
-            }
-            tc::fence_async_smem();
-            tc::fence_before();
-            ptx::named_bar_sync(3, 128);
-            if (r == 0) ptx::mbar_arrive(&b.sready);
-
-            // ---- dS, dz of this chunk ----
+            // ---- dS, dz of this chunk; then the stage is no longer read here or by MMA4 ----
             la_wait(b, &b.dsfull, par, p);
             tc::fence_after();
             __syncwarp();
@@ -540,12 +569,22 @@ k_linattn(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtens
                 tc::ld2(tmem + lane_base + COL_DS + 64, dz, dz1);
                 z += dz;
             }
-            if (c == nc - 1 && p.S_out != nullptr && !aborted(b)) {
-                float4 *dst = reinterpret_cast<float4 *>(p.S_out + ((h * 2 + half) * 64 + k) * 64);
+            if (r == 0) ptx::mbar_arrive(&b.empty[s]);
+            if (c == nc - 1) {   // end of a head: its final state, then the next head's start
+                if (p.S_out != nullptr && !aborted(b)) {
+                    float4 *dst = reinterpret_cast<float4 *>(p.S_out + ((h * 2 + half) * 64 + k) * 64);
 #pragma unroll
-                for (int q4 = 0; q4 < 16; ++q4)
-                    dst[q4] = make_float4(S[4 * q4], S[4 * q4 + 1], S[4 * q4 + 2], S[4 * q4 + 3]);
-                p.z_out[(h * 2 + half) * 64 + k] = z;
+                    for (int q4 = 0; q4 < 16; ++q4)
+                        dst[q4] = make_float4(S[4 * q4], S[4 * q4 + 1], S[4 * q4 + 2], S[4 * q4 + 3]);
+                    p.z_out[(h * 2 + half) * 64 + k] = z;
+                }
+                if (g + 1 < total) load_start(h + gridDim.x);
+            }
+
+            // ---- the next chunk's state, once MMA3 of this chunk has read the buffer ----
+            if (g + 1 < total) {
+                la_wait(b, &b.ofull, par, p);
+                publish_state();
             }
         }
     }
