@@ -219,21 +219,26 @@ __device__ bool lookforward(const BwdParams &p, int64_t head, int64_t c, Suffix<
     return true;
 }
 
-// Rows per block (chunk) of the backward kernel: K, V, O and dO of a chunk
-// fill about 64 KB of shared memory.
+// Rows per block (chunk) of the backward kernel: K, dO and one shared slot
+// for O and then V of a chunk fill at most about 64 KB of shared memory.  O
+// is read only for the per-token dot products g . o at the start, V only in
+// the rescan after the look-forward, so V is copied into O's slot once every
+// warp is done with O (the copy overlaps the look-forward).
 template <int D, typename Tin, typename Tout>
 struct BwdTile {
-    static constexpr int ROW_BYTES = D * (2 * int(sizeof(Tin)) + 2 * int(sizeof(Tout)));
+    static constexpr int OV_ELEM = int(sizeof(Tin)) > int(sizeof(Tout)) ? int(sizeof(Tin)) : int(sizeof(Tout));
+    static constexpr int ROW_BYTES = D * (int(sizeof(Tin)) + OV_ELEM + int(sizeof(Tout)));
     static constexpr int WARPS_RAW = 65536 / (32 * ROW_BYTES);
     static constexpr int WARPS = WARPS_RAW < 1 ? 1 : (WARPS_RAW > 4 ? 4 : WARPS_RAW);
     static constexpr int C = 32 * WARPS;
     static constexpr int SS = StateLayout<D>::SS;
     static constexpr size_t in_bytes = size_t(C) * D * sizeof(Tin);
     static constexpr size_t out_bytes = size_t(C) * D * sizeof(Tout);
+    static constexpr size_t ov_bytes = size_t(C) * D * OV_ELEM;
     static constexpr size_t k_off = 0;
-    static constexpr size_t v_off = k_off + in_bytes;
-    static constexpr size_t o_off = v_off + in_bytes;
-    static constexpr size_t g_off = o_off + out_bytes;
+    static constexpr size_t o_off = k_off + in_bytes;   // O, then V
+    static constexpr size_t v_off = o_off;
+    static constexpr size_t g_off = o_off + ov_bytes;
     static constexpr size_t wst_off = g_off + out_bytes;                         // [WARPS][SS]
     static constexpr size_t cst_off = wst_off + size_t(WARPS) * SS * sizeof(float);
     static constexpr size_t cf_off = cst_off + size_t(WARPS) * SS * sizeof(float); // [WARPS][32] float4
@@ -367,14 +372,13 @@ __global__ void __launch_bounds__(BwdTile<D, Tin, Tout>::WARPS * 32) k_scan_bwd(
     unsigned *my_flag = p.flags + chunk;
     float *my_state = p.states + size_t(chunk) * 2 * SS;
 
-    // K, V, O, dO rows of the chunk into shared memory
+    // K, O, dO rows of the chunk into shared memory (V follows into O's slot)
+    const unsigned bi = static_cast<unsigned>(nvalid) * D * sizeof(Tin);
     if (tid == 0) {
-        const unsigned bi = static_cast<unsigned>(nvalid) * D * sizeof(Tin);
         const unsigned bo = static_cast<unsigned>(nvalid) * D * sizeof(Tout);
-        ptx::mbar_arrive_expect_tx(bar, 2 * bi + 2 * bo);
+        ptx::mbar_arrive_expect_tx(bar, bi + 2 * bo);
         const uint64_t pol = ptx::policy_evict_first();
         ptx::bulk_g2s(Ks, static_cast<const Tin *>(p.K) + row0 * D, bi, bar, pol);
-        ptx::bulk_g2s(Vs, static_cast<const Tin *>(p.V) + row0 * D, bi, bar, pol);
         ptx::bulk_g2s(Os, static_cast<const Tout *>(p.O) + row0 * D, bo, bar, pol);
         ptx::bulk_g2s(Gs, static_cast<const Tout *>(p.dO) + row0 * D, bo, bar, pol);
     }
@@ -476,7 +480,13 @@ __global__ void __launch_bounds__(BwdTile<D, Tin, Tout>::WARPS * 32) k_scan_bwd(
         }
         suffix_store<D>(wst + warp * SS, a, lane);
     }
+    // every warp is done with O: V into its slot, during the look-forward
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     __syncthreads();
+    if (tid == 0) {
+        ptx::mbar_arrive_expect_tx(bar, bi);
+        ptx::bulk_g2s(Vs, static_cast<const Tin *>(p.V) + row0 * D, bi, bar, ptx::policy_evict_first());
+    }
 
     // 3. chunk aggregate, look-forward, inclusive suffix, per-warp carries
     if (warp == 0) {
@@ -519,7 +529,14 @@ __global__ void __launch_bounds__(BwdTile<D, Tin, Tout>::WARPS * 32) k_scan_bwd(
         }
     }
     __syncthreads();
+    // V has landed (a block never leaves with its copy in flight)
+    const bool v_loaded = wait_bar(bar, 1, p.wait_limit_ns);
     if (*s_abort) return;
+    if (__syncthreads_or(!v_loaded)) {
+        if (tid == 0) atomicOr(p.status, STATUS_LOAD_TIMEOUT);
+        wait_bar(bar, 1, p.wait_limit_ns);
+        return;
+    }
 
     // 4. rescan the warp's rows from the last to the first
     float dsv = 0.f;   // dL/ds of this lane's token
