@@ -450,14 +450,11 @@ template <typename Tout>
 aaren_status_t launch_linattn(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                               const la::Params &p, cudaStream_t st)
 {
-    static bool configured = false;
-    if (!configured) {
-        if (cudaFuncSetAttribute(la::k_linattn<Tout>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 la::kSmemBytes) != cudaSuccess)
-            return AAREN_ERR_CUDA;
-        configured = true;
-    }
-    const int64_t grid = p.BH < sm_count() ? p.BH : sm_count();
+    static std::atomic<unsigned long long> configured{0};   // per device
+    if (allow_smem(la::k_linattn<Tout>, la::kSmemBytes, configured) != cudaSuccess) return AAREN_ERR_CUDA;
+    const int sms = sm_count();
+    if (sms <= 0) return AAREN_ERR_CUDA;
+    const int64_t grid = p.BH < sms ? p.BH : sms;   // persistent: one CTA per SM, heads strided over them
     la::k_linattn<Tout><<<static_cast<unsigned>(grid), la::kThreads, la::kSmemBytes, st>>>(tq, tk, tv, p);
     return cudaGetLastError() == cudaSuccess ? AAREN_OK : AAREN_ERR_CUDA;
 }
