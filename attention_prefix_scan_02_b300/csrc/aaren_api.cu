@@ -138,10 +138,12 @@ aaren_status_t launch_scan(const ScanParams &p, int64_t total_chunks, cudaStream
 #ifndef AAREN_PIPE_STAGES_D64
 #define AAREN_PIPE_STAGES_D64 4
 #endif
-template <int D>
+template <int D, typename Tin = __nv_bfloat16>
 struct PipeChoice {
-    static constexpr int GROUPS = (D == 128) ? AAREN_PIPE_GROUPS_D128 : (D == 64 ? AAREN_PIPE_GROUPS_D64 : 4);
-    static constexpr int STAGES = (D == 128) ? AAREN_PIPE_STAGES_D128 : (D == 64 ? AAREN_PIPE_STAGES_D64 : 4);
+    // float32 at d = 64 has the stage size of bfloat16 at d = 128 (64 KB)
+    static constexpr int DE = (sizeof(Tin) == 4) ? 2 * D : D;
+    static constexpr int GROUPS = (DE == 128) ? AAREN_PIPE_GROUPS_D128 : (DE == 64 ? AAREN_PIPE_GROUPS_D64 : 4);
+    static constexpr int STAGES = (DE == 128) ? AAREN_PIPE_STAGES_D128 : (DE == 64 ? AAREN_PIPE_STAGES_D64 : 4);
 };
 
 int sm_count()
@@ -152,13 +154,13 @@ int sm_count()
     return n;
 }
 
-template <int D, typename Tout>
+template <int D, typename Tout, typename Tin = __nv_bfloat16>
 aaren_status_t launch_pipe(const ScanParams &p, int64_t total_chunks, cudaStream_t st)
 {
-    using PC = PipeChoice<D>;
-    using Tile = PipeTile<D, PC::GROUPS, PC::STAGES>;
+    using PC = PipeChoice<D, Tin>;
+    using Tile = PipeTile<D, PC::GROUPS, PC::STAGES, Tin>;
     static std::atomic<unsigned long long> configured{0};
-    auto kern = k_scan_pipe<D, Tout, PC::GROUPS, PC::STAGES>;
+    auto kern = k_scan_pipe<D, Tout, PC::GROUPS, PC::STAGES, Tin>;
     if (allow_smem(kern, Tile::smem_bytes, configured) != cudaSuccess) return AAREN_ERR_CUDA;
     int per_sm = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, Tile::THREADS,
@@ -178,7 +180,11 @@ aaren_status_t dispatch_scan_dtype(const ScanParams &p, int64_t total, int32_t d
                                    cudaStream_t st)
 {
     switch (dtype) {
-    case AAREN_F32: return launch_scan<D, float, float>(p, total, st);
+    case AAREN_F32:
+        // float32 d = 64 (a 64 KB stage, as bfloat16 at d = 128) runs on the
+        // persistent kernel; other float32 sizes on the one-chunk-per-block one
+        if constexpr (D == 64) return launch_pipe<D, float, float>(p, total, st);
+        else return launch_scan<D, float, float>(p, total, st);
 #ifdef AAREN_BF16_BLOCK_KERNEL
     case AAREN_BF16: return launch_scan<D, __nv_bfloat16, __nv_bfloat16>(p, total, st);
     case AAREN_BF16_F32OUT: return launch_scan<D, __nv_bfloat16, float>(p, total, st);

@@ -45,6 +45,7 @@
 
 #include <cuda_bf16.h>
 #include <cstdint>
+#include <type_traits>
 
 #include "common.cuh"
 #include "ptx.cuh"
@@ -66,9 +67,9 @@ constexpr int kPipeFoldBatch = AAREN_PIPE_FOLD_BATCH;
 constexpr int kRescanBlock = AAREN_PIPE_RESCAN_BLOCK;
 static_assert(32 % kRescanBlock == 0, "rescan blocks must tile the warp's 32 rows");
 
-template <int D, int GROUPS_, int STAGES_>
+template <int D, int GROUPS_, int STAGES_, typename Tin_ = __nv_bfloat16>
 struct PipeTile {
-    using Tin = __nv_bfloat16;
+    using Tin = Tin_;
     static constexpr int GROUPS = GROUPS_;
     static constexpr int STAGES = STAGES_;
     static constexpr int C = 32 * kPipeComputeWarps;   // tokens per chunk
@@ -113,6 +114,51 @@ template <int E>
 struct RawRow {
     unsigned w[E == 4 ? 2 : 1];
 };
+
+// E float32 values of one row held in registers (float32 keys and values).
+template <int E>
+struct RawRowF {
+    float v[E];
+};
+
+template <typename Tin, int E>
+using PipeRow = typename std::conditional<sizeof(Tin) == 4, RawRowF<E>, RawRow<E>>::type;
+
+template <int E>
+__device__ __forceinline__ void lds_row(const float *p, RawRowF<E> &r)
+{
+    if constexpr (E == 4) {
+        const float4 v = *reinterpret_cast<const float4 *>(p);
+        r.v[0] = v.x; r.v[1] = v.y; r.v[2] = v.z; r.v[3] = v.w;
+    } else if constexpr (E == 2) {
+        const float2 v = *reinterpret_cast<const float2 *>(p);
+        r.v[0] = v.x; r.v[1] = v.y;
+    } else {
+        r.v[0] = *p;
+    }
+}
+
+template <int E>
+__device__ __forceinline__ void zero_row(RawRowF<E> &r)
+{
+#pragma unroll
+    for (int e = 0; e < E; ++e) r.v[e] = 0.f;
+}
+
+template <int E>
+__device__ __forceinline__ void zero_row(RawRow<E> &r)
+{
+#pragma unroll
+    for (int k = 0; k < (E == 4 ? 2 : 1); ++k) r.w[k] = 0u;
+}
+
+// float32 rows need no unpacking (the zero register is unused)
+template <int E>
+__device__ __forceinline__ void unpack_row_late(const RawRowF<E> &r, unsigned, float (&f)[E])
+{
+#pragma unroll
+    for (int e = 0; e < E; ++e) f[e] = r.v[e];
+}
 
 template <int E>
 __device__ __forceinline__ void lds_row(const __nv_bfloat16 *p, RawRow<E> &r)
@@ -219,13 +265,12 @@ __device__ __forceinline__ bool compute_wait(uint64_t *bar, unsigned parity, int
     return AAREN_PIPE_SPIN_WAIT ? wait_bar_spin(bar, parity, limit_ns) : wait_bar(bar, parity, limit_ns);
 }
 
-template <int D, typename Tout, int GROUPS, int STAGES>
-__global__ void __launch_bounds__(PipeTile<D, GROUPS, STAGES>::THREADS, 1)
+template <int D, typename Tout, int GROUPS, int STAGES, typename Tin = __nv_bfloat16>
+__global__ void __launch_bounds__(PipeTile<D, GROUPS, STAGES, Tin>::THREADS, 1)
     k_scan_pipe(const ScanParams p, const int64_t total_chunks)
 {
-    using Tin = __nv_bfloat16;
     using L = VLayout<D>;
-    using T = PipeTile<D, GROUPS, STAGES>;
+    using T = PipeTile<D, GROUPS, STAGES, Tin>;
     constexpr int E = L::E;
     constexpr int C = T::C;
     constexpr int SS = T::SS;
@@ -475,6 +520,14 @@ __global__ void __launch_bounds__(PipeTile<D, GROUPS, STAGES>::THREADS, 1)
         const Tin *Kw = reinterpret_cast<const Tin *>(stage) + size_t(wg) * 32 * D + lane * E;
         const Tin *Vw = reinterpret_cast<const Tin *>(stage + T::st_v) + size_t(wg) * 32 * D + lane * E;
         float s = -INFINITY;
+        if constexpr (sizeof(Tin) == 4) {
+            // float32 keys: lane = token, the compensated dot product of the
+            // one-chunk-per-block kernel and the backward pass (the same
+            // function, so every kernel sees bitwise the same score)
+            const float *qs = reinterpret_cast<const float *>(stage + T::st_q);
+            if (lane < nv)
+                s = dot_row<D, Tin>(reinterpret_cast<const Tin *>(stage) + size_t(wg * 32 + lane) * D, qs, lane);
+        } else {
 #pragma unroll 1
         for (int quarter = 0; quarter < 4; ++quarter) {
             float x[8];
@@ -495,6 +548,7 @@ __global__ void __launch_bounds__(PipeTile<D, GROUPS, STAGES>::THREADS, 1)
             }
             const float sr = transpose_sum8(x, lane);
             if ((lane >> 3) == quarter) s = sr;
+        }
         }
         if (lane >= nv) s = -INFINITY;
 
@@ -527,11 +581,10 @@ __global__ void __launch_bounds__(PipeTile<D, GROUPS, STAGES>::THREADS, 1)
 
         // V rows into registers (for the rescan); then hand the stage back to
         // the pool (compute warp 0, once all four warps are done with it)
-        RawRow<E> vr[32];
+        PipeRow<Tin, E> vr[32];
 #pragma unroll
         for (int r = 0; r < 32; ++r) {
-#pragma unroll
-            for (int k = 0; k < (E == 4 ? 2 : 1); ++k) vr[r].w[k] = 0u;
+            zero_row<E>(vr[r]);
             if (owns && r < nv) lds_row<E>(Vw + size_t(r) * D, vr[r]);
         }
         __syncwarp();

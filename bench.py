@@ -478,7 +478,7 @@ def run_ours(args):
                      "algorithmic_bytes_per_launch": alg_bytes, "launch_ms": mean_launch_ms,
                      "peak_source": peak_src,
                      "kernel": "k_scan_reduce" if reduce else "k_scan_bwd" if backward else
-                               ("k_scan_pipe" if wl.dtype == "bf16" else "k_scan_fwd")},
+                               ("k_scan_pipe" if (wl.dtype == "bf16" or wl.d == 64) else "k_scan_fwd")},
         "cpu_baseline": cpu,
         "e2e": e2e,
         "clocks": clocks.summary(),
