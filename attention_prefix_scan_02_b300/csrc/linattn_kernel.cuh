@@ -24,14 +24,17 @@
 // The ones column appended to V makes MMA4 also produce dz and MMA2 the
 // intra-chunk row sums of A; z appended to S makes MMA3 produce Q'_i . z:
 // every denominator term comes out of the same products as its numerator.
-// Every rounded operand (A, the weighted keys, S) is carried as a bfloat16
-// pair hi + lo = x to about 2^-17 relative, so products are float32-accurate;
-// Q', K' and V are exact bfloat16 inputs.
+// Every rounded operand (A, the weighted keys, S, z) is carried as a
+// bfloat16 pair hi + lo = x to within 2^-16 relative (hi the truncation, lo
+// the rounded remainder), so products are float32-accurate; Q', K' and V are
+// exact bfloat16 inputs.
 //
 // One persistent CTA per SM walks whole heads (h = blockIdx.x, += gridDim.x)
 // chunk by chunk (g counts this CTA's chunks).  Roles:
 //   warp 0, one thread   tiled TMA loads of Q, K, V (two stages)
-//   warp 1, one thread   issues the MMAs as their operands become ready
+//   warp 1, one thread   issues the MMAs as their operands become ready: MMA1,
+//       then MMA4, MMA3 and MMA2 in whatever order their inputs arrive (one
+//       commit for MMA4, one for MMA3 + MMA2)
 //   two row warpgroups (warps 4-7 and 8-11, thread = token row i = TMEM
 //       lane; warpgroup hf takes columns 64hf.. of P and dims 32hf.. of O):
 //       ReLU of Q and K in place (half of each row each); P -> A (causal
