@@ -181,3 +181,14 @@ def test_linattn_argument_checks(lib):
     assert call(O=ptr + 8) == binding.AAREN_ERR_INVALID          # misaligned output
     assert call(B=0) == binding.AAREN_OK                         # nothing to do
     assert call(N=1 << 31) == binding.AAREN_ERR_INVALID          # beyond the 32-bit coordinates
+
+
+def test_linattn_binding_rejects_host_tensors_and_bad_shapes():
+    """The binding marshals only: it refuses host tensors (there is no CPU
+    path) and mismatched shapes before calling the library."""
+    import torch
+    x = torch.zeros(1, 1, 8, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA"):
+        binding.aaren_linattn_forward(x, x, x, x.clone(), 8.0)
+    with pytest.raises(ValueError, match="CUDA"):
+        binding.linattn_forward(x, x, x)

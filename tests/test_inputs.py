@@ -78,3 +78,33 @@ def test_batch_offset_draws_a_shard_of_a_larger_batch():
     for r in range(3):
         q, K, V = inputs.batch_inputs(small, b0=r)
         assert torch.equal(q[0], qb[r]) and torch.equal(K[0], Kb[r]) and torch.equal(V[0], Vb[r])
+
+
+def test_token_recipe_matches_heads_and_shards():
+    """One query per token (the linear-attention workload): the batch tensors
+    equal the per-head draws for any thread count, bf16 values are the
+    rounded float32 draws, queries differ per token, and b0 selects a shard
+    of a larger batch."""
+    wl = inputs.custom(2, 3, 40, 64, dtype="bf16", seed=5, kind="tokens")
+    Q1, K1, V1 = inputs.token_inputs(wl, threads=1)
+    Q4, K4, V4 = inputs.token_inputs(wl, threads=4)
+    assert Q1.shape == (2, 3, 40, 64) and Q1.dtype == torch.bfloat16
+    assert torch.equal(Q1, Q4) and torch.equal(K1, K4) and torch.equal(V1, V4)
+    Qh, Kh, Vh = inputs.head_token_inputs(wl, 1, 2)
+    assert np.array_equal(Q1[1, 2].float().numpy(), Qh)
+    assert np.array_equal(K1[1, 2].float().numpy(), Kh)
+    assert np.array_equal(V1[1, 2].float().numpy(), Vh)
+    assert np.array_equal(inputs.round_bf16(Qh), Qh)
+    assert not np.array_equal(Qh[0], Qh[1])
+    big = inputs.custom(4, 3, 40, 64, dtype="bf16", seed=5, kind="tokens")
+    Qs, Ks, Vs = inputs.token_inputs(big, b0=0)
+    sub = inputs.custom(2, 3, 40, 64, dtype="bf16", seed=5, kind="tokens")
+    Qb, Kb, Vb = inputs.token_inputs(sub, b0=2)
+    assert torch.equal(Qs[2:], Qb) and torch.equal(Ks[2:], Kb) and torch.equal(Vs[2:], Vb)
+
+
+def test_linattn_workload_shape():
+    wl = inputs.WORKLOADS["linattn"]
+    assert (wl.B, wl.H, wl.N, wl.d, wl.dtype, wl.kind) == (64, 16, 2048, 64, "bf16", "tokens")
+    # 1024 heads over 148 SMs: the busiest SM takes 7 heads against 6.9 on average
+    assert -(-wl.heads // 148) == 7
