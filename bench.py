@@ -256,6 +256,26 @@ def cpu_oracle_rate(wl, tokens_per_head, threads, min_s=0.0):
     return passes * len(heads) * n / dt, dt, n, passes
 
 
+def cpu_oracle_single_rate(wl, tokens, min_s=1.0):
+    """The float64 oracle on the calling thread alone: the first `tokens`
+    tokens of the first head, repeated until `min_s` seconds have elapsed.
+    Returns (head-tokens/s, seconds, tokens, passes)."""
+    import oracle
+    from attention_prefix_scan_02_b300 import inputs
+    n = min(tokens, wl.N)
+    sub = inputs.custom(1, 1, n, wl.d, wl.dtype, wl.seed, wl.kind, wl.name)
+    q, K, V = inputs.head_inputs(sub, 0, 0)
+    passes = 0
+    t0 = time.perf_counter()
+    while True:
+        oracle.scan(q, K, V)
+        passes += 1
+        dt = time.perf_counter() - t0
+        if dt >= min_s or passes >= CPU_SAMPLE_MAX_PASSES:
+            break
+    return passes * n / dt, dt, n, passes
+
+
 def host_cores():
     try:
         return len(os.sched_getaffinity(0))
@@ -322,6 +342,9 @@ def run_ours(args):
                "sample": f"the first {n} tokens of all {wl.heads} heads ({n * wl.heads} head-tokens), "
                          f"{passes} passes, {dt:.1f} s wall on {threads} threads "
                          f"(about {dt * threads:.0f} CPU-seconds)"}
+        r1, dt1, n1, passes1 = cpu_oracle_single_rate(wl, CPU_SAMPLE_TOKENS // 4, CPU_SAMPLE_MIN_S)
+        cpu["single_thread"] = {"value": r1, "unit": "head-tokens/s", "cores": 1,
+                                "sample": f"the first {n1} tokens of head 0, {passes1} passes, {dt1:.1f} s"}
 
     # rank r draws batch entries [r B, (r + 1) B) of the recipe: the ranks
     # together process a batch of world * B sequences (weak scaling)
@@ -406,6 +429,7 @@ def run_ours(args):
         raise SystemExit(f"device status error in the timed region: {binding.status_string(status)}")
     launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     mean_launch_ms = statistics.mean(launch_ms)
+    launch_spread = {"launch_ms_median": statistics.median(launch_ms), "launch_ms_min": min(launch_ms)}
     step_ms = mean_launch_ms if flush is not None else t_start.elapsed_time(t_end) / args.steps
     step_ms = max_over_ranks(step_ms, dist, "cuda")
 
@@ -476,7 +500,7 @@ def run_ours(args):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "algorithmic_bytes_per_launch": alg_bytes, "launch_ms": mean_launch_ms,
-                     "peak_source": peak_src,
+                     **launch_spread, "peak_source": peak_src,
                      "kernel": "k_scan_reduce" if reduce else "k_scan_bwd" if backward else
                                ("k_scan_pipe" if (wl.dtype == "bf16" or wl.d == 64) else "k_scan_fwd")},
         "cpu_baseline": cpu,
@@ -645,6 +669,9 @@ def run_linattn(args):
         cpu = {"value": rate, "unit": "head-tokens/s", "cores": threads, "kind": "oracle",
                "sample": f"the first {n} tokens of {nh} heads ({n * nh} head-tokens), {passes} passes, "
                          f"{dt:.1f} s wall on {threads} threads"}
+        r1, dt1, n1, nh1, passes1 = la_cpu_rate(wl, LA_CPU_TOKENS, 1, 1, CPU_SAMPLE_MIN_S)
+        cpu["single_thread"] = {"value": r1, "unit": "head-tokens/s", "cores": 1,
+                                "sample": f"the first {n1} tokens of head 0, {passes1} passes, {dt1:.1f} s"}
     Q, K, V = inputs.token_inputs(wl, device="cuda", b0=rank * wl.B)
     O = torch.empty(K.shape, dtype=out_t, device="cuda")
     stream = torch.cuda.current_stream()
@@ -680,7 +707,9 @@ def run_linattn(args):
     status = binding.aaren_check()
     if status != binding.AAREN_OK:
         raise SystemExit(f"device status error in the timed region: {binding.status_string(status)}")
-    mean_launch_ms = statistics.mean(s.elapsed_time(e) for s, e in zip(starts, ends))
+    launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    mean_launch_ms = statistics.mean(launch_ms)
+    launch_spread = {"launch_ms_median": statistics.median(launch_ms), "launch_ms_min": min(launch_ms)}
     step_ms = max_over_ranks(t_start.elapsed_time(t_end) / args.steps, dist, "cuda")
     tokens = wl.heads * wl.N
     elems = tokens * wl.d
@@ -731,7 +760,7 @@ def run_linattn(args):
                      "frac": achieved / peak,
                      "traffic": profiled_traffic(wl, out, "linattn_bf16_traffic.json", "k_linattn"),
                      "algorithmic_bytes_per_launch": alg_bytes, "launch_ms": mean_launch_ms,
-                     "peak_source": peak_src, "kernel": "k_linattn"},
+                     **launch_spread, "peak_source": peak_src, "kernel": "k_linattn"},
         "cpu_baseline": cpu,
         "e2e": {"value": whole_job_rate(tokens, world, e2e_ms), "unit": "head-tokens/s",
                 "h2d_bytes_per_step": 3 * elems * 2, "d2h_bytes_per_step": elems * out_b,
