@@ -16,9 +16,9 @@
 //     and lane l owns dims [E l, E l + E) of every row:
 //       - scores: each lane forms its E-term share of q . k_t per row, then a
 //         transposed butterfly of shuffles leaves s_t on lane t;
-//       - V of the warp's rows is copied into registers (still bfloat16) and
-//         the stage is handed back at once ("empty" mbarrier);
-//       - warp aggregate (m, u, w) into shared memory ("agg" mbarrier);
+//       - V of the warp's rows is copied into registers (still bfloat16);
+//       - warp aggregate (m, u, w) from those registers into shared memory
+//         ("agg" mbarrier), and the stage is handed back ("empty" mbarrier);
 //       - after the carry arrives ("carry" mbarrier): rescan from registers
 //         and write O;
 //   * one carry warp that never holds V:
@@ -552,8 +552,17 @@ __global__ void __launch_bounds__(PipeTile<D, GROUPS, STAGES, Tin>::THREADS, 1)
         }
         if (lane >= nv) s = -INFINITY;
 
-        // 2. warp aggregate (m_w, u_w, w_w) relative to the warp's maximum,
-        //    V read from the stage
+        // 2. V rows into registers (for the aggregate and the rescan), then
+        //    the warp aggregate (m_w, u_w, w_w), relative to the warp's
+        //    maximum, from those registers: the stage is read once for V and
+        //    the aggregate, on which every successor's look-back waits, is
+        //    out sooner.  Rows past nv are zero and weigh 0.
+        PipeRow<Tin, E> vr[32];
+#pragma unroll
+        for (int r = 0; r < 32; ++r) {
+            zero_row<E>(vr[r]);
+            if (owns && r < nv) lds_row<E>(Vw + size_t(r) * D, vr[r]);
+        }
         const float mw = warp_max(s);
         const float b = (s == -INFINITY) ? 0.f : exp_rel(s, mw);
         const float ww = warp_sum(b);
@@ -561,16 +570,11 @@ __global__ void __launch_bounds__(PipeTile<D, GROUPS, STAGES, Tin>::THREADS, 1)
             float u[E];
 #pragma unroll
             for (int e = 0; e < E; ++e) u[e] = 0.f;
-#pragma unroll 4
-            for (int r = 0; r < nv; ++r) {
+#pragma unroll
+            for (int r = 0; r < 32; ++r) {
                 const float br = __shfl_sync(kFull, b, r);
                 float v[E];
-                if (owns) {
-                    load_vals<E>(Vw + size_t(r) * D, v);
-                } else {
-#pragma unroll
-                    for (int e = 0; e < E; ++e) v[e] = 0.f;
-                }
+                unpack_row_late<E>(vr[r], 0u, v);
 #pragma unroll
                 for (int e = 0; e < E; ++e) u[e] = fmaf(br, v[e], u[e]);
             }
@@ -579,14 +583,8 @@ __global__ void __launch_bounds__(PipeTile<D, GROUPS, STAGES, Tin>::THREADS, 1)
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(aggb);
 
-        // V rows into registers (for the rescan); then hand the stage back to
-        // the pool (compute warp 0, once all four warps are done with it)
-        PipeRow<Tin, E> vr[32];
-#pragma unroll
-        for (int r = 0; r < 32; ++r) {
-            zero_row<E>(vr[r]);
-            if (owns && r < nv) lds_row<E>(Vw + size_t(r) * D, vr[r]);
-        }
+        // then hand the stage back to the pool (compute warp 0, once all four
+        // warps are done with it)
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(empty);
         if (wg == 0) {

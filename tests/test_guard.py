@@ -9,8 +9,11 @@ final state or its workspace fails here.  The inputs must be unchanged too.
 
 The guarded outputs are also compared with the same call on plain
 allocations, which shows the kernel wrote the whole output and nothing
-depends on where it sits; their values against the oracle are the parity
-tests' business."""
+depends on where it sits: bitwise where the combination order is fixed (the
+reduce, the linear attention, the step), and to rounding where a decoupled
+look-back folds whatever mix of aggregates and inclusive prefixes it finds
+at run time (the forward scan and its final state).  Their values against
+the oracle are the parity tests' business."""
 import math
 
 import pytest
@@ -53,6 +56,13 @@ def _same(a, b):
     torch.testing.assert_close(a.float(), b.float(), rtol=0, atol=0, equal_nan=True)
 
 
+def _close(a, b):
+    """Equal up to the rounding of a different combination order: a few
+    float32 ulps, or one bfloat16 ulp of the output."""
+    rtol = 2 ** -7 if a.dtype == torch.bfloat16 else 1e-5
+    torch.testing.assert_close(a.float(), b.float(), rtol=rtol, atol=1e-6)
+
+
 DTYPES = [(torch.float32, torch.float32), (torch.bfloat16, torch.bfloat16),
           (torch.bfloat16, torch.float32)]
 SIZES = [1, 3, 33, 129, 300]
@@ -80,13 +90,13 @@ def test_scan_forward_writes_stay_in_bounds(d, io):
                       torch.empty(B * H, device="cuda"))
         binding.aaren_scan_forward_ex(q, K, V, Op, m_out=mp, u_out=up, w_out=wp)
         assert binding.aaren_check() == binding.AAREN_OK
-        _same(O.t, Op); _same(m.t, mp); _same(u.t, up); _same(w.t, wp)
+        _close(O.t, Op); _close(m.t, mp); _close(u.t, up); _close(w.t, wp)
 
         On = Guarded((B, H, N, d), out_t)
         binding.aaren_scan_forward_noalloc(q, K, V, On.t)
         assert binding.aaren_check() == binding.AAREN_OK
         assert On.intact(), f"noalloc O guard band overwritten at N={N}, d={d}"
-        _same(On.t, Op)
+        _close(On.t, Op)
 
 
 @pytest.mark.parametrize("d", [16, 64, 128])
