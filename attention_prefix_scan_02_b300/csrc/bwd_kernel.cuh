@@ -424,9 +424,19 @@ __global__ void __launch_bounds__(BwdTile<D, Tin, Tout>::WARPS * 32) k_scan_bwd(
     } else {
         s = rows_dot<D, Tin>(qv, Kw, nv, lane);
     }
-    float delta;
+    // g_t . o_t (both rows from shared memory), and in the same pass the R
+    // part of the warp aggregate, sum_t c_t g_t with c_t = e^{lse_0 - lse_t}
+    // relative to the warp's first row: the weights need only the saved
+    // (m, w), so each g row is read once and the aggregate, which the
+    // predecessors' look-forwards wait on, is ready sooner.  Rows past nv
+    // are zero and weigh 0.
+    const bool valid = lane < nv;
+    const float am0 = __shfl_sync(kFull, mt, 0), aw0 = __shfl_sync(kFull, wt, 0);
+    const float cw = valid ? lse_ratio(am0, aw0, mt, wt) : 0.f;
+    float delta, Ragg[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) Ragg[e] = 0.f;
     {
-        // g_t . o_t: both rows from shared memory
         float x8[8];
         delta = 0.f;
 #pragma unroll 1
@@ -435,8 +445,11 @@ __global__ void __launch_bounds__(BwdTile<D, Tin, Tout>::WARPS * 32) k_scan_bwd(
             for (int i = 0; i < 8; ++i) {
                 const int r = quarter * 8 + i;
                 x8[i] = 0.f;
+                float gf[E];
+#pragma unroll
+                for (int e = 0; e < E; ++e) gf[e] = 0.f;
                 if (owns && r < nv) {
-                    float gf[E], of[E];
+                    float of[E];
                     load_vals<E>(Gw + size_t(r) * D + lane * E, gf);
                     load_vals<E>(Ow + size_t(r) * D + lane * E, of);
                     float acc = gf[0] * of[0];
@@ -444,37 +457,25 @@ __global__ void __launch_bounds__(BwdTile<D, Tin, Tout>::WARPS * 32) k_scan_bwd(
                     for (int e = 1; e < E; ++e) acc = fmaf(gf[e], of[e], acc);
                     x8[i] = acc;
                 }
+                const float cr = __shfl_sync(kFull, cw, r);
+#pragma unroll
+                for (int e = 0; e < E; ++e) Ragg[e] = fmaf(cr, gf[e], Ragg[e]);
             }
             const float sr = bwd_transpose_sum8<float>(x8, lane);
             if ((lane >> 3) == quarter) delta = sr;
         }
     }
-    const bool valid = lane < nv;
     const float pw = valid ? exp_rel(s, mt) / wt : 0.f;
 
     // 2. warp aggregate: sums relative to lse at the warp's first row
     {
         Suffix<E> a;
         if (nv > 0) {
-            a.m = __shfl_sync(kFull, mt, 0);
-            a.w = __shfl_sync(kFull, wt, 0);
-            const float cw = valid ? lse_ratio(a.m, a.w, mt, wt) : 0.f;
+            a.m = am0;
+            a.w = aw0;
             a.D = warp_sum(cw * delta);
 #pragma unroll
-            for (int e = 0; e < E; ++e) a.R[e] = 0.f;
-#pragma unroll 4
-            for (int r = 0; r < nv; ++r) {
-                const float cr = __shfl_sync(kFull, cw, r);
-                float gf[E];
-                if (owns) {
-                    load_vals<E>(Gw + size_t(r) * D + lane * E, gf);
-                } else {
-#pragma unroll
-                    for (int e = 0; e < E; ++e) gf[e] = 0.f;
-                }
-#pragma unroll
-                for (int e = 0; e < E; ++e) a.R[e] = fmaf(cr, gf[e], a.R[e]);
-            }
+            for (int e = 0; e < E; ++e) a.R[e] = Ragg[e];
         } else {
             suffix_empty<E>(a);
         }
