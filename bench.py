@@ -102,10 +102,11 @@ def workload(args):
     return wl
 
 
-# a GPU spin queued after each L2 flush, ahead of the launch's start event:
-# about 0.15 ms at 2 GHz, longer than the host needs to issue the launch, so
-# the GPU never idles inside the timed window waiting for it
-FLUSH_SPIN_CYCLES = 300_000
+# a GPU spin queued ahead of a start event (before the first timed launch,
+# and after each L2 flush): about 0.15 ms at 2 GHz, longer than the host
+# needs to issue the launch, so the GPU never idles inside the timed window
+# waiting for it.  The spin itself is outside every timed window.
+SPIN_CYCLES = 300_000
 
 
 def needs_flush(wl):
@@ -120,7 +121,7 @@ def flush_l2(flush):
     spin so the next launch is already queued when its start event runs."""
     import torch
     flush.fill_(1.0)
-    torch.cuda._sleep(FLUSH_SPIN_CYCLES)
+    torch.cuda._sleep(SPIN_CYCLES)
 
 
 def describe(wl, out):
@@ -434,6 +435,7 @@ def run_ours(args):
         clocks.begin = time.time()
         t_start = torch.cuda.Event(enable_timing=True)
         t_end = torch.cuda.Event(enable_timing=True)
+        torch.cuda._sleep(SPIN_CYCLES)   # the host issues the first launches meanwhile
         t_start.record(stream)
         for i in range(args.steps):
             if flush is not None:
@@ -716,6 +718,7 @@ def run_linattn(args):
         clocks.begin = time.time()
         t_start = torch.cuda.Event(enable_timing=True)
         t_end = torch.cuda.Event(enable_timing=True)
+        torch.cuda._sleep(SPIN_CYCLES)   # the host issues the first launches meanwhile
         t_start.record(stream)
         for i in range(args.steps):
             starts[i].record(stream)
