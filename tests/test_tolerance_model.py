@@ -1,0 +1,107 @@
+"""Where the linear attention's 1e-4 tolerance comes from, checked on the CPU.
+
+The tensor-core path multiplies bfloat16 operands with float32 accumulation.
+Q', K' and V are exact bfloat16 inputs, but four operands are rounded
+values: the weighted scores A_ij = (Q'_i . K'_j) cos(theta (i - j)), the
+cos / sin weighted keys, and the state S (with z).  Each is carried as a
+pair hi + lo: hi the bfloat16 truncation, lo the round-to-nearest bfloat16
+of the remainder, about 16 significant bits together.
+
+This file models that arithmetic in numpy: float32 products and sums, the
+same chunking (128 tokens) and the same splits.  It checks it against the
+float64 oracle on the shapes of the linattn workload (N = 2048, d = 64,
+M = N).  Two facts fix the tolerance:
+  * with every pair kept, the row-wise error stays well inside 1e-4;
+  * dropping the low half of any one pair pushes it past 1e-4.
+So the GPU parity bound of 1e-4 holds for a correct kernel and fails for
+one that loses any low half.  The model shares no code with the CUDA path.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+C = 128
+BOUND = 1e-4
+
+
+def _bf16(x):
+    """Round float32 to the nearest bfloat16 (ties to even), as float32."""
+    t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32))
+    return t.to(torch.bfloat16).to(torch.float32).numpy()
+
+
+def _trunc(x):
+    """The bfloat16 truncation of float32 values (their top 16 bits)."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32) & np.uint32(0xFFFF0000)
+    return u.view(np.float32)
+
+
+def _pair(x, keep_lo):
+    hi = _trunc(x)
+    lo = _bf16((x - hi).astype(np.float32)) if keep_lo else np.zeros_like(hi)
+    return hi, lo
+
+
+def _mm(a, b):
+    return np.matmul(a.astype(np.float32), b.astype(np.float32), dtype=np.float32)
+
+
+def model(Q, K, V, M, lo_A=True, lo_S=True, lo_K=True):
+    """The chunked form with hi/lo operand pairs, in float32."""
+    N, d = Q.shape
+    theta = np.float32(np.pi / 2 / M)
+    S = {"c": np.zeros((d, d + 1), np.float32), "s": np.zeros((d, d + 1), np.float32)}
+    O = np.zeros((N, d), np.float32)
+    idx = np.arange(C)
+    W = np.cos((idx[:, None] - idx[None, :]).astype(np.float64) * float(theta)).astype(np.float32)
+    W = np.where(idx[:, None] >= idx[None, :], W, np.float32(0))
+    for t0 in range(0, N, C):
+        n = min(C, N - t0)
+        Qp = np.maximum(Q[t0:t0 + n], 0)
+        Kp = np.maximum(K[t0:t0 + n], 0)
+        V1 = np.concatenate([V[t0:t0 + n], np.ones((n, 1), np.float32)], axis=1)
+        pos = np.arange(t0 + 1, t0 + n + 1, dtype=np.float64) * float(theta)
+        cs, sn = np.cos(pos).astype(np.float32), np.sin(pos).astype(np.float32)
+        A = (_mm(Qp, Kp.T) * W[:n, :n]).astype(np.float32)
+        Ah, Al = _pair(A, lo_A)
+        acc = _mm(Ah, V1) + _mm(Al, V1)
+        for part, w in (("c", cs), ("s", sn)):
+            Sh, Sl = _pair(S[part], lo_S)
+            acc = acc + w[:, None] * (_mm(Qp, Sh) + _mm(Qp, Sl))
+        den = acc[:, d]
+        safe = np.where(den != 0, den, np.float32(1))
+        O[t0:t0 + n] = np.where(den[:, None] != 0, acc[:, :d] / safe[:, None], np.float32(0))
+        for part, w in (("c", cs), ("s", sn)):
+            Kh, Kl = _pair((Kp * w[:, None]).astype(np.float32), lo_K)
+            S[part] = S[part] + _mm(Kh.T, V1) + _mm(Kl.T, V1)
+    return O
+
+
+def rowwise(a, b):
+    num = np.max(np.abs(a.astype(np.float64) - b), axis=1)
+    den = np.maximum(np.max(np.abs(b), axis=1), 1e-30)
+    return float(np.max(num / den))
+
+
+@pytest.fixture(scope="module")
+def heads():
+    r = np.random.default_rng(5)
+    out = []
+    for _ in range(2):
+        Q, K, V = (_bf16(r.standard_normal((2048, 64)).astype(np.float32)) for _ in range(3))
+        ref, _ = oracle.la_scan(Q, K, V, 2048.0)
+        out.append((Q, K, V, ref))
+    return out
+
+
+def test_all_pairs_kept_stays_well_inside_the_bound(heads):
+    err = max(rowwise(model(Q, K, V, 2048.0), ref) for Q, K, V, ref in heads)
+    assert err < BOUND / 3, err
+
+
+@pytest.mark.parametrize("drop", ["lo_A", "lo_S", "lo_K"])
+def test_dropping_any_low_half_breaks_the_bound(heads, drop):
+    err = max(rowwise(model(Q, K, V, 2048.0, **{drop: False}), ref) for Q, K, V, ref in heads)
+    assert err > BOUND, (drop, err)
