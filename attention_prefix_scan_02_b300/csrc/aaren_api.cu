@@ -914,13 +914,19 @@ extern "C" aaren_status_t aaren_scan_forward_noalloc(const void *q, const void *
                                                      void *O, int64_t B, int64_t H, int64_t N,
                                                      int64_t d, int32_t dtype, void *stream)
 {
+    // Sizes first: a problem whose workspace exceeds the array is rejected
+    // before any pointer is looked at or any CUDA call is made.
+    if (!supported_dtype(dtype) || !supported_d(d)) return AAREN_ERR_UNSUPPORTED;
+    if (B < 0 || H < 0 || N < 0) return AAREN_ERR_INVALID;
+    const size_t need = aaren_scan_workspace_bytes(B, H, N, d);
+    if (need == SIZE_MAX) return AAREN_ERR_INVALID;   // the shape overflows
+    if (need > AAREN_NOALLOC_SCRATCH_BYTES) return AAREN_ERR_WORKSPACE;
     void *scratch = nullptr;
     const aaren_status_t rc = noalloc_scratch(&scratch);
     if (rc != AAREN_OK) return rc;
-    // The regular path with a caller workspace allocates nothing: it zeroes
-    // the ticket and flags of the workspace (cudaMemsetAsync) and launches.
-    // A problem whose workspace exceeds the array is rejected there with
-    // AAREN_ERR_WORKSPACE before anything is launched.
+    // The regular path with a caller workspace allocates nothing: it checks
+    // the pointers, zeroes the ticket and flags of the workspace
+    // (cudaMemsetAsync) and launches.
     return aaren_scan_forward_ex(q, K, V, O, B, H, N, d, dtype, nullptr, nullptr, nullptr, nullptr,
                                  nullptr, nullptr, scratch, AAREN_NOALLOC_SCRATCH_BYTES, stream);
 }

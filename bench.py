@@ -43,8 +43,7 @@ sys.path.insert(0, ROOT)
 FALLBACK_HBM_GBS = 6400.0
 CPU_SAMPLE_TOKENS = 1 << 18      # per head, cpu_baseline leg
 CPU_SAMPLE_MIN_S = 1.0           # cpu_baseline: repeat the sample until this much wall time
-CPU_SAMPLE_MAX_PASSES = 12
-REF_STEP_TOKENS = 1 << 16        # per head, --impl reference steps
+CPU_SAMPLE_MAX_PASSES = 100000   # passes are bounded by time (CPU_SAMPLE_MIN_S), not count
 METRIC = "Aaren scan tokens/s and achieved HBM GB/s (% of B300 peak), 1 GPU"
 
 
@@ -155,9 +154,12 @@ def kernel_source_hash(kernel):
 def profiled_traffic(wl, out, record="scan_long_bf16_traffic.json", kernel="k_scan_pipe"):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
     on the current source of the kernel with this head size, dtype and output
-    type; else None.  The capture is of a smaller case (the full launch is
-    too large for a multi-pass capture); its bytes per head-token are scaled
-    to this launch's head-tokens."""
+    type; else None.  When the capture is of a smaller case (the full launch
+    is too large for a multi-pass capture), reads are scaled to this launch's
+    head-tokens (every input byte is read once, so reads grow in proportion),
+    and writes are the algorithmic output bytes less the capture's write
+    shortfall: the tail of the output still in L2 when the kernel ends, a
+    fixed residue of the L2's size, not a per-token rate."""
     path = os.path.join(ROOT, "profiles", record)
     try:
         with open(path) as f:
@@ -168,8 +170,15 @@ def profiled_traffic(wl, out, record="scan_long_bf16_traffic.json", kernel="k_sc
         return None
     if (rec.get("d") != wl.d or rec.get("in_dtype") != wl.dtype or rec.get("out_dtype") != out):
         return None
-    per_token = rec.get("dram_bytes_per_head_token")
-    return None if per_token is None else int(per_token * wl.heads * wl.N)
+    try:
+        cap_tokens = rec["head_tokens"]
+        alg_w = rec["algorithmic_write_bytes_per_head_token"]
+        reads = rec["dram_bytes_read"] / cap_tokens * wl.heads * wl.N
+        residue = max(0.0, cap_tokens * alg_w - rec["dram_bytes_write"])
+        writes = max(0.0, wl.heads * wl.N * alg_w - residue)
+    except (KeyError, TypeError, ZeroDivisionError):
+        return None
+    return int(reads + writes)
 
 
 def measured_peak():
@@ -250,53 +259,81 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows), "samples_taken": where}
 
 
-def cpu_oracle_rate(wl, tokens_per_head, threads, min_s=0.0):
-    """Time the float64 oracle (as it stands) over `tokens_per_head` leading
-    tokens of every head, heads spread over `threads` host threads, repeating
-    the pass until `min_s` seconds have elapsed.  Inputs are drawn before the
-    clock starts.  Returns (head-tokens/s, seconds, tokens per head, passes)."""
-    from concurrent.futures import ThreadPoolExecutor
+class OracleTimer:
+    """The float64 oracle, as it stands, timed on this host's cores.  `items`
+    holds one head's inputs each; `fn(item, out)` runs the oracle on one head
+    writing its output into `out`.  Inputs are drawn, every output array is
+    allocated and first-touched, and the thread pool is started (one untimed
+    pass) before any clock starts, so a timed pass is the oracle's own work.
+    run(min_s) repeats whole passes over the items until `min_s` seconds have
+    elapsed and returns (head-tokens/s, seconds, passes)."""
 
-    import oracle
-    from attention_prefix_scan_02_b300 import inputs
-    n = min(tokens_per_head, wl.N)
-    sub = inputs.custom(wl.B, wl.H, n, wl.d, wl.dtype, wl.seed, wl.kind, wl.name)
-    heads = [inputs.head_inputs(sub, b, h) for b in range(wl.B) for h in range(wl.H)]
+    def __init__(self, fn, items, tokens, d, threads):
+        import numpy as np
+        from concurrent.futures import ThreadPoolExecutor
+        self.fn, self.items, self.tokens, self.threads = fn, items, tokens, threads
+        self.outs = [np.ones((tokens, d), dtype=np.float64) for _ in items]
+        self.pool = ThreadPoolExecutor(max_workers=threads) if threads > 1 else None
+        self.one_pass()
 
-    def one(x):
-        q, K, V = x
-        oracle.scan(q, K, V)      # O is computed and discarded
+    def _one(self, i):
+        self.fn(self.items[i], self.outs[i])
 
-    passes = 0
-    t0 = time.perf_counter()
-    with ThreadPoolExecutor(max_workers=threads) as ex:
+    def one_pass(self):
+        if self.pool is None:
+            for i in range(len(self.items)):
+                self._one(i)
+        else:
+            list(self.pool.map(self._one, range(len(self.items))))
+
+    def run(self, min_s):
+        passes = 0
+        t0 = time.perf_counter()
         while True:
-            list(ex.map(one, heads))
+            self.one_pass()
             passes += 1
             dt = time.perf_counter() - t0
             if dt >= min_s or passes >= CPU_SAMPLE_MAX_PASSES:
                 break
-    return passes * len(heads) * n / dt, dt, n, passes
+        return passes * len(self.items) * self.tokens / dt, dt, passes
+
+    def close(self):
+        if self.pool is not None:
+            self.pool.shutdown()
+        self.outs = []
 
 
-def cpu_oracle_single_rate(wl, tokens, min_s=1.0):
-    """The float64 oracle on the calling thread alone: the first `tokens`
-    tokens of the first head, repeated until `min_s` seconds have elapsed.
-    Returns (head-tokens/s, seconds, tokens, passes)."""
+def scan_oracle_timer(wl, tokens_per_head, threads, heads=None):
+    """OracleTimer over the first `tokens_per_head` tokens of the first
+    `heads` heads (all by default) of workload `wl`."""
     import oracle
     from attention_prefix_scan_02_b300 import inputs
-    n = min(tokens, wl.N)
-    sub = inputs.custom(1, 1, n, wl.d, wl.dtype, wl.seed, wl.kind, wl.name)
-    q, K, V = inputs.head_inputs(sub, 0, 0)
-    passes = 0
-    t0 = time.perf_counter()
-    while True:
-        oracle.scan(q, K, V)
-        passes += 1
-        dt = time.perf_counter() - t0
-        if dt >= min_s or passes >= CPU_SAMPLE_MAX_PASSES:
-            break
-    return passes * n / dt, dt, n, passes
+    n = min(tokens_per_head, wl.N)
+    sub = inputs.custom(wl.B, wl.H, n, wl.d, wl.dtype, wl.seed, wl.kind, wl.name)
+    hs = [(b, h) for b in range(wl.B) for h in range(wl.H)][:heads or wl.heads]
+    items = [inputs.head_inputs(sub, b, h) for b, h in hs]
+    return OracleTimer(lambda x, out: oracle.scan(*x, out=out), items, n, wl.d, min(threads, len(items)))
+
+
+def cpu_baseline_leg(wl, threads):
+    """The oracle on the scan workload's sample: all host threads over the
+    first CPU_SAMPLE_TOKENS tokens of every head, and one thread over the
+    first CPU_SAMPLE_TOKENS / 4 tokens of head 0."""
+    t = scan_oracle_timer(wl, CPU_SAMPLE_TOKENS, threads)
+    rate, dt, passes = t.run(CPU_SAMPLE_MIN_S)
+    n, nh, used = t.tokens, len(t.items), t.threads
+    t.close()
+    cpu = {"value": rate, "unit": "head-tokens/s", "cores": used, "kind": "oracle",
+           "sample": f"the first {n} tokens of all {nh} heads ({n * nh} head-tokens), "
+                     f"{passes} passes, {dt:.1f} s wall on {used} threads "
+                     f"(about {dt * used:.0f} CPU-seconds)"}
+    t1 = scan_oracle_timer(wl, CPU_SAMPLE_TOKENS // 4, 1, heads=1)
+    r1, dt1, passes1 = t1.run(CPU_SAMPLE_MIN_S)
+    t1.close()
+    cpu["single_thread"] = {"value": r1, "unit": "head-tokens/s", "cores": 1,
+                            "sample": f"the first {t1.tokens} tokens of head 0, {passes1} passes, "
+                                      f"{dt1:.1f} s"}
+    return cpu
 
 
 def host_cores():
@@ -307,27 +344,34 @@ def host_cores():
 
 
 def run_reference(args):
+    """The oracle arm: the float64 oracle timed on this host's cores, one
+    step = repeated passes over the cpu_baseline leg's sample (the first
+    CPU_SAMPLE_TOKENS tokens of every head, one thread per head) for at
+    least CPU_SAMPLE_MIN_S seconds, so the two report one measurement."""
     rank, world, _ = dist_env()
     if rank != 0:
         return 0
     wl = workload(args)
     out = args.out_dtype or wl.dtype
-    cores = host_cores()
-    threads = min(cores, wl.heads)
+    threads = min(host_cores(), wl.heads)
+    timer = scan_oracle_timer(wl, CPU_SAMPLE_TOKENS, threads)
     rates = []
     for i in range(args.warmup + args.steps):
-        r, dt, n, _ = cpu_oracle_rate(wl, REF_STEP_TOKENS, threads)
+        r, dt, passes = timer.run(CPU_SAMPLE_MIN_S if i >= args.warmup else 0.0)
         if i >= args.warmup:
-            rates.append((r, dt))
-    n = min(REF_STEP_TOKENS, wl.N)
-    sample = f"each step: the first {n} tokens of all {wl.heads} heads ({n * wl.heads} head-tokens)"
-    value = statistics.mean(r for r, _ in rates)
+            rates.append((r, dt, passes))
+    n, nh, used = timer.tokens, len(timer.items), timer.threads
+    timer.close()
+    sample = (f"each step: passes over the first {n} tokens of all {nh} heads ({n * nh} head-tokens) "
+              f"for at least {CPU_SAMPLE_MIN_S:.0f} s on {used} threads "
+              f"({statistics.mean(p for _, _, p in rates):.1f} passes a step on average)")
+    value = statistics.mean(r for r, _, _ in rates)
     line = {"impl": "reference", "metric": METRIC,
             "value": value, "unit": "head-tokens/s", "n_gpus": args.gpus, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": 1e3 * statistics.mean(dt for _, dt in rates),
+            "warmup": args.warmup, "ms_per_step": 1e3 * statistics.mean(dt for _, dt, _ in rates),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": describe(wl, out),
-            "cpu_baseline": {"value": value, "unit": "head-tokens/s", "cores": threads,
+            "cpu_baseline": {"value": value, "unit": "head-tokens/s", "cores": used,
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": "head-tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
@@ -358,16 +402,7 @@ def run_ours(args):
     # CPU baseline first (host memory is freed before the GPU legs)
     cpu = None
     if rank == 0:
-        cores = host_cores()
-        threads = min(cores, wl.heads)
-        rate, dt, n, passes = cpu_oracle_rate(wl, CPU_SAMPLE_TOKENS, threads, CPU_SAMPLE_MIN_S)
-        cpu = {"value": rate, "unit": "head-tokens/s", "cores": threads, "kind": "oracle",
-               "sample": f"the first {n} tokens of all {wl.heads} heads ({n * wl.heads} head-tokens), "
-                         f"{passes} passes, {dt:.1f} s wall on {threads} threads "
-                         f"(about {dt * threads:.0f} CPU-seconds)"}
-        r1, dt1, n1, passes1 = cpu_oracle_single_rate(wl, CPU_SAMPLE_TOKENS // 4, CPU_SAMPLE_MIN_S)
-        cpu["single_thread"] = {"value": r1, "unit": "head-tokens/s", "cores": 1,
-                                "sample": f"the first {n1} tokens of head 0, {passes1} passes, {dt1:.1f} s"}
+        cpu = cpu_baseline_leg(wl, min(host_cores(), wl.heads))
 
     # rank r draws batch entries [r B, (r + 1) B) of the recipe: the ranks
     # together process a batch of world * B sequences (weak scaling)
@@ -517,7 +552,7 @@ def run_ours(args):
         "unit": "head-tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": warmup, "ms_per_step": step_ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f32", "data": "synthetic",
+        "dtype": "f32", "io_dtype": f"{wl.dtype} in, {out} out", "data": "synthetic",
         "config": dict(describe(wl, out), op=args.op, global_batch=world * wl.B,
                        parallelism=f"independent sequences, {world} rank(s), no collective"),
         "gpu_launches": args.steps,
@@ -635,33 +670,18 @@ LA_CPU_TOKENS = 512        # oracle sample: leading tokens of each sampled head
 LA_CPU_HEADS = 64
 
 
-def la_cpu_rate(wl, tokens, heads, threads, min_s=0.0):
-    """Time the float64 linear-attention oracle (as it stands) on the first
-    `tokens` tokens of the first `heads` heads, spread over `threads` host
-    threads, repeated until `min_s` seconds have elapsed.  Returns
-    (head-tokens/s, seconds, tokens, heads, passes)."""
-    from concurrent.futures import ThreadPoolExecutor
-
+def la_oracle_timer(wl, tokens, heads, threads):
+    """OracleTimer for the float64 linear-attention oracle over the first
+    `tokens` tokens of the first `heads` heads of workload `wl`."""
     import oracle
     from attention_prefix_scan_02_b300 import inputs
     n = min(tokens, wl.N)
     sub_wl = inputs.custom(wl.B, wl.H, n, wl.d, wl.dtype, wl.seed, wl.kind, wl.name)
     hs = [(b, h) for b in range(wl.B) for h in range(wl.H)][:heads]
-    data = [inputs.head_token_inputs(sub_wl, b, h) for b, h in hs]
-
-    def one(x):
-        oracle.la_scan(*x, float(wl.N))
-
-    passes = 0
-    t0 = time.perf_counter()
-    with ThreadPoolExecutor(max_workers=threads) as ex:
-        while True:
-            list(ex.map(one, data))
-            passes += 1
-            dt = time.perf_counter() - t0
-            if dt >= min_s or passes >= CPU_SAMPLE_MAX_PASSES:
-                break
-    return passes * len(data) * n / dt, dt, n, len(data), passes
+    items = [inputs.head_token_inputs(sub_wl, b, h) for b, h in hs]
+    M = float(wl.N)
+    return OracleTimer(lambda x, out: oracle.la_scan(*x, M, out=out), items, n, wl.d,
+                       min(threads, len(items)))
 
 
 def run_linattn(args):
@@ -688,14 +708,19 @@ def run_linattn(args):
     warmup = max(3, args.warmup)
     cpu = None
     if rank == 0:
-        threads = min(host_cores(), LA_CPU_HEADS)
-        rate, dt, n, nh, passes = la_cpu_rate(wl, LA_CPU_TOKENS, LA_CPU_HEADS, threads, CPU_SAMPLE_MIN_S)
-        cpu = {"value": rate, "unit": "head-tokens/s", "cores": threads, "kind": "oracle",
+        t = la_oracle_timer(wl, LA_CPU_TOKENS, LA_CPU_HEADS, host_cores())
+        rate, dt, passes = t.run(CPU_SAMPLE_MIN_S)
+        n, nh, used = t.tokens, len(t.items), t.threads
+        t.close()
+        cpu = {"value": rate, "unit": "head-tokens/s", "cores": used, "kind": "oracle",
                "sample": f"the first {n} tokens of {nh} heads ({n * nh} head-tokens), {passes} passes, "
-                         f"{dt:.1f} s wall on {threads} threads"}
-        r1, dt1, n1, nh1, passes1 = la_cpu_rate(wl, LA_CPU_TOKENS, 1, 1, CPU_SAMPLE_MIN_S)
+                         f"{dt:.1f} s wall on {used} threads"}
+        t1 = la_oracle_timer(wl, LA_CPU_TOKENS, 1, 1)
+        r1, dt1, passes1 = t1.run(CPU_SAMPLE_MIN_S)
+        t1.close()
         cpu["single_thread"] = {"value": r1, "unit": "head-tokens/s", "cores": 1,
-                                "sample": f"the first {n1} tokens of head 0, {passes1} passes, {dt1:.1f} s"}
+                                "sample": f"the first {t1.tokens} tokens of head 0, {passes1} passes, "
+                                          f"{dt1:.1f} s"}
     Q, K, V = inputs.token_inputs(wl, device="cuda", b0=rank * wl.B)
     O = torch.empty(K.shape, dtype=out_t, device="cuda")
     stream = torch.cuda.current_stream()
@@ -807,21 +832,25 @@ def main():
             return 0
         from attention_prefix_scan_02_b300 import inputs
         wl = inputs.WORKLOADS["linattn"]
-        threads = min(host_cores(), LA_CPU_HEADS)
+        timer = la_oracle_timer(wl, LA_CPU_TOKENS, LA_CPU_HEADS, host_cores())
         rates = []
         for i in range(args.warmup + args.steps):
-            r, dt, n, nh, _ = la_cpu_rate(wl, LA_CPU_TOKENS, LA_CPU_HEADS, threads)
+            r, dt, passes = timer.run(CPU_SAMPLE_MIN_S if i >= args.warmup else 0.0)
             if i >= args.warmup:
                 rates.append((r, dt))
+        n, nh, used = timer.tokens, len(timer.items), timer.threads
+        timer.close()
         value = statistics.mean(r for r, _ in rates)
         print(json.dumps({"impl": "reference", "metric": METRIC + " (causal cos-re-weighted linear attention)",
                           "value": value, "unit": "head-tokens/s", "n_gpus": args.gpus, "steps": args.steps,
                           "warmup": args.warmup, "ms_per_step": 1e3 * statistics.mean(dt for _, dt in rates),
                           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
                           "data": "synthetic", "config": {"workload": "linattn", "op": "linattn"},
-                          "cpu_baseline": {"value": value, "unit": "head-tokens/s", "cores": threads,
+                          "cpu_baseline": {"value": value, "unit": "head-tokens/s", "cores": used,
                                            "kind": "oracle",
-                                           "sample": f"each step: the first {n} tokens of {nh} heads"},
+                                           "sample": f"each step: passes over the first {n} tokens of {nh} "
+                                                     f"heads for at least {CPU_SAMPLE_MIN_S:.0f} s on "
+                                                     f"{used} threads"},
                           "e2e": {"value": value, "unit": "head-tokens/s", "h2d_bytes_per_step": 0,
                                   "d2h_bytes_per_step": 0}}), flush=True)
         return 0

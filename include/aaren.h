@@ -211,7 +211,13 @@ size_t aaren_reduce_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t d);
 
 /*
  * aaren_state_init -- set n states to the identity (m = -inf, u = 0, w = 0),
- * the state of an empty prefix, before the first aaren_step.
+ * the state of an empty prefix, before the first aaren_step: the RNN of the
+ * "Attention as an RNN" review ("Proposed method") starts from an empty
+ * state and takes one token per update; in the running sums of the
+ * "Self-attention Does Not Need O(n^2) Memory" review (section 2
+ * "Algorithm": v* and s* start at zero) with the maximum of section 3
+ * "Numerical Stability" subtracted, the empty prefix has no maximum yet,
+ * hence m = -inf.
  *   m [n], u [n,d], w [n]   float32, written.
  * Errors: AAREN_ERR_INVALID, AAREN_ERR_UNSUPPORTED, AAREN_ERR_CUDA.
  */
@@ -325,12 +331,26 @@ int64_t aaren_scan_chunk_tokens(int64_t d, int32_t dtype);
  * Limits and behaviour:
  *  - A problem whose workspace, aaren_scan_workspace_bytes(B,H,N,d), exceeds
  *    AAREN_NOALLOC_SCRATCH_BYTES is rejected with AAREN_ERR_WORKSPACE before
- *    anything runs (with d = 128 that is one to two million tokens over all
- *    heads, depending on the dtype's chunk size; smaller d allow more).
+ *    any pointer is read or any CUDA call is made (with d = 128 that is one
+ *    to two million tokens over all heads, depending on the dtype's chunk
+ *    size; smaller d allow more).  Unsupported d or dtype and negative sizes
+ *    are rejected first, as by aaren_scan_forward.
  *  - No cudaMalloc, cudaFree or other allocating call is made.  The part of
  *    the array that must start at zero is cleared on `stream` by every call.
- *  - The first call on a device looks up the array's device address (once per
- *    device); make that first call before any stream capture.
+ *  - When the array takes its memory: with CUDA's lazy module loading (the
+ *    default) the library's device code, this array included, is loaded on
+ *    a device the first time any entry point of this library launches a
+ *    kernel or looks up a device symbol there; with eager loading
+ *    (CUDA_MODULE_LOADING=EAGER) when the library's module is loaded on that
+ *    device's context.  Either way the 16 MiB stay reserved until the
+ *    process exits.
+ *  - The first call of this entry point on a device looks up the array's
+ *    device address and keeps it for the rest of the process (once per
+ *    device).  Make that first call before any stream capture.
+ *  - Devices with ordinals 0..63 only (AAREN_ERR_CUDA beyond).
+ *  - Do not call it on a device after cudaDeviceReset of that device in the
+ *    same process: the reset unloads the module, and the kept address would
+ *    name memory that no longer holds the array.
  *  - All calls on a device share the one array, which keeps the last call's
  *    contents: calls whose executions overlap on the GPU (different streams
  *    without ordering between them) race and corrupt each other's results.

@@ -133,12 +133,19 @@ def scan_scores(s, V, init=None, want_O=True):
     return O, float(m[0]), u, float(w[0])
 
 
-def scan(q, K, V, init=None, want_O=True):
-    """One head: scores then recurrence.  Returns (O [N,d] or None, m, u [d], w)."""
+def scan(q, K, V, init=None, want_O=True, out=None):
+    """One head: scores then recurrence.  Returns (O [N,d] or None, m, u [d], w).
+    `out` (optional, float64 C-contiguous [N, d]) receives O in place of a
+    fresh array."""
     q, K, V = _f32(q), _f32(K), _f32(V)
     N, d = K.shape
     m0, u0, w0 = _init_arrays(init, d)
-    O = np.empty((N, d), dtype=np.float64) if want_O else None
+    if out is not None:
+        if out.dtype != np.float64 or out.shape != (N, d) or not out.flags.c_contiguous:
+            raise ValueError("out must be a C-contiguous float64 array of shape [N, d]")
+        O = out
+    else:
+        O = np.empty((N, d), dtype=np.float64) if want_O else None
     m = np.empty(1); w = np.empty(1); u = np.empty(d)
     rc = _load().oracle_scan(_p32(q), _p32(K), _p32(V), N, d, _p64(m0), _p64(u0),
                              _p64(w0), _p64(O), _p64(m), _p64(u), _p64(w))
@@ -290,13 +297,20 @@ def la_bruteforce(Q, K, V, M):
     return O
 
 
-def la_scan(Q, K, V, M, init=None, pos0=0, want_O=True):
+def la_scan(Q, K, V, M, init=None, pos0=0, want_O=True, out=None):
     """The same output by the decomposed prefix sums, O(N d^2).  init =
     (Sc, Ss, zc, zs) continues a scan whose last token had position pos0.
-    Returns (O [N,d] or None, (Sc [d,d], Ss [d,d], zc [d], zs [d]))."""
+    Returns (O [N,d] or None, (Sc [d,d], Ss [d,d], zc [d], zs [d])).  `out`
+    (optional, float64 C-contiguous [N, d]) receives O in place of a fresh
+    array."""
     Q, K, V = _f32(Q), _f32(K), _f32(V)
     N, d = K.shape
-    O = np.empty((N, d)) if want_O else None
+    if out is not None:
+        if out.dtype != np.float64 or out.shape != (N, d) or not out.flags.c_contiguous:
+            raise ValueError("out must be a C-contiguous float64 array of shape [N, d]")
+        O = out
+    else:
+        O = np.empty((N, d)) if want_O else None
     Sc = np.empty((d, d)); Ss = np.empty((d, d)); zc = np.empty(d); zs = np.empty(d)
     ini = [None] * 4 if init is None else [_f64(x) for x in init]
     if _load().oracle_la_scan(_p32(Q), _p32(K), _p32(V), N, d, float(M), int(pos0),

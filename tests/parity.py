@@ -17,6 +17,8 @@ Readings of "max relative error" (the plainest well-posed ones):
 import numpy as np
 import torch
 
+import oracle
+
 TOL_F32 = 2e-5     # float32 inputs and outputs
 TOL_BF16 = 2e-3    # bfloat16 inputs, float32 accumulation, float32 output
 
@@ -73,3 +75,25 @@ def state_errors(m, u, w, m_ref, u_ref, w_ref):
     ew = float(np.max(np.abs(w * f - w_ref) / w_ref))
     eu = rowwise_rel(u * f[:, None], u_ref)
     return em, ew, eu
+
+
+def compare_head_by_blocks(O_head, q, K, V, bf16_out, rows=1 << 16):
+    """One head's whole output O_head (a CPU tensor [N, d]) against the
+    oracle, `rows` tokens at a time.  At each block boundary the oracle
+    continues from its own float64 state, which is the same arithmetic as one
+    pass over the head, so host memory stays bounded at any N.
+    Returns (row-wise relative error, bf16 ulp violations (0 unless
+    bf16_out), all finite, the oracle's final state (m, u, w))."""
+    N = K.shape[0]
+    state = None
+    err, bad, finite = 0.0, 0, True
+    for r0 in range(0, N, rows):
+        r1 = min(N, r0 + rows)
+        Oref, m, u, w = oracle.scan(q, K[r0:r1], V[r0:r1], init=state)
+        state = (m, u, w)
+        blk = O_head[r0:r1]
+        finite = finite and bool(torch.isfinite(blk.float()).all())
+        err = max(err, rowwise_rel(blk.float(), Oref))
+        if bf16_out:
+            bad += bf16_ulp_violations(blk, Oref)
+    return err, bad, finite, state
