@@ -9,6 +9,7 @@ or fails to load, every call raises.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 
@@ -16,14 +17,16 @@ import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libaaren.so")
+CHECKED_LIB_PATH = os.path.join(_HERE, "libaaren_checked.so")   # -DAAREN_CHECKED build
 
 AAREN_OK = 0
 AAREN_ERR_INVALID = 1
 AAREN_ERR_UNSUPPORTED = 2
 AAREN_ERR_CUDA = 3
 AAREN_ERR_LOOKBACK_TIMEOUT = 4
-AAREN_ERR_LOAD_TIMEOUT = 5
-AAREN_ERR_WORKSPACE = 6
+AAREN_ERR_BOUNDS = 5
+AAREN_ERR_LOAD_TIMEOUT = 6
+AAREN_ERR_WORKSPACE = 7
 
 AAREN_F32 = 0
 AAREN_BF16 = 1
@@ -36,7 +39,8 @@ EXPORTS = (
     "aaren_abi_version", "aaren_debug_set_fault", "aaren_scan_chunk_tokens",
     "aaren_scan_forward_noalloc", "aaren_scan_reduce", "aaren_reduce_workspace_bytes",
     "aaren_scan_forward_stats", "aaren_scan_backward", "aaren_backward_workspace_bytes",
-    "aaren_linattn_forward",
+    "aaren_linattn_forward", "aaren_debug_drop_arrival", "aaren_backward_chunk_tokens",
+    "aaren_checked_build", "aaren_debug_bounds_probe",
 )
 
 # size of the fixed device scratch of aaren_scan_forward_noalloc (include/aaren.h)
@@ -87,6 +91,14 @@ def load(path: str | None = None):
     lib.aaren_debug_set_fault.restype = _i32
     lib.aaren_scan_chunk_tokens.argtypes = [_i64, _i32]
     lib.aaren_scan_chunk_tokens.restype = _i64
+    lib.aaren_debug_drop_arrival.argtypes = [_i64]
+    lib.aaren_debug_drop_arrival.restype = _i32
+    lib.aaren_backward_chunk_tokens.argtypes = [_i64, _i32]
+    lib.aaren_backward_chunk_tokens.restype = _i64
+    lib.aaren_checked_build.argtypes = []
+    lib.aaren_checked_build.restype = _i32
+    lib.aaren_debug_bounds_probe.argtypes = [_i64]
+    lib.aaren_debug_bounds_probe.restype = _i32
     lib.aaren_scan_forward_noalloc.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i32, _vp]
     lib.aaren_scan_forward_noalloc.restype = _i32
     lib.aaren_scan_reduce.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i32,
@@ -108,6 +120,19 @@ def load(path: str | None = None):
     if path is None:
         _lib = lib
     return lib
+
+
+@contextlib.contextmanager
+def using_library(path: str):
+    """Route every call of this module to another build of the library (the
+    tests run the checked build, libaaren_checked.so, this way)."""
+    global _lib
+    prev = _lib
+    _lib = load(path)
+    try:
+        yield _lib
+    finally:
+        _lib = prev
 
 
 def status_string(code: int) -> str:
@@ -170,6 +195,10 @@ def aaren_scan_workspace_bytes(B: int, H: int, N: int, d: int) -> int:
 
 def aaren_scan_chunk_tokens(d: int, dtype: int) -> int:
     return int(load().aaren_scan_chunk_tokens(d, dtype))
+
+
+def aaren_backward_chunk_tokens(d: int, dtype: int) -> int:
+    return int(load().aaren_backward_chunk_tokens(d, dtype))
 
 
 def aaren_scan_forward(q, K, V, O, stream=None):
@@ -337,6 +366,18 @@ def aaren_check(stream=None) -> int:
 def aaren_debug_set_fault(never_publish_chunk: int = -1, wait_limit_ns: int = 0):
     _raise(load().aaren_debug_set_fault(never_publish_chunk, wait_limit_ns),
            "aaren_debug_set_fault")
+
+
+def aaren_debug_drop_arrival(chunk: int = -1):
+    _raise(load().aaren_debug_drop_arrival(chunk), "aaren_debug_drop_arrival")
+
+
+def aaren_debug_bounds_probe(offset: int = 0):
+    _raise(load().aaren_debug_bounds_probe(offset), "aaren_debug_bounds_probe")
+
+
+def aaren_checked_build() -> bool:
+    return bool(load().aaren_checked_build())
 
 
 def aaren_abi_version() -> int:

@@ -30,6 +30,8 @@ namespace {
 
 constexpr int64_t kDefaultWaitLimitNs = 1000000000;   // 1 s
 std::atomic<int64_t> g_fault_chunk{-1};
+std::atomic<int64_t> g_drop_chunk{-1};
+std::atomic<int64_t> g_bounds_probe{0};
 std::atomic<int64_t> g_wait_limit_ns{kDefaultWaitLimitNs};
 
 constexpr size_t kHeaderBytes = 256;   // ticket counter, padded
@@ -517,6 +519,7 @@ aaren_status_t aaren_linattn_forward(const void *Q, const void *K, const void *V
     p.inv_2M = 1.0 / (2.0 * M);
     p.status = status;
     p.wait_limit_ns = g_wait_limit_ns.load();
+    p.drop_chunk = g_drop_chunk.load();
     return dtype == AAREN_BF16 ? launch_linattn<__nv_bfloat16>(tq, tk, tv, p, st)
                                : launch_linattn<float>(tq, tk, tv, p, st);
 }
@@ -604,6 +607,7 @@ static aaren_status_t scan_forward_impl(const void *q, const void *K, const void
             p.heads = BH;
             p.chunks_per_head = wl.chunks_per_head;
             p.fault_chunk = g_fault_chunk.load();
+            p.drop_chunk = g_drop_chunk.load();
             p.wait_limit_ns = g_wait_limit_ns.load();
             rc = dispatch_scan(p, wl.total_chunks, d, dtype, st);
         }
@@ -692,6 +696,7 @@ aaren_status_t aaren_scan_backward(const void *q, const void *K, const void *V, 
             p.N = N;
             p.heads = BH;
             p.chunks_per_head = wl.chunks_per_head;
+            p.fault_chunk = g_fault_chunk.load();
             p.wait_limit_ns = g_wait_limit_ns.load();
             rc = dispatch_bwd(p, wl.total_chunks, d, dtype, st);
         }
@@ -760,6 +765,14 @@ aaren_status_t aaren_scan_reduce(const void *q, const void *K, const void *V, vo
         p.heads = BH;
         p.P = 1;
         p.seg = kReduceRows;
+        p.part_slots = BH * rl.P_max;
+        p.status = nullptr;
+#ifdef AAREN_CHECKED
+        if (cudaGetSymbolAddress(reinterpret_cast<void **>(&p.status), g_status) != cudaSuccess) {
+            if (owned) cudaFreeAsync(ws, st);
+            return AAREN_ERR_CUDA;
+        }
+#endif
         rc = dispatch_reduce(p, rl.P_max, d, dtype, st);
     }
     if (owned && cudaFreeAsync(ws, st) != cudaSuccess && rc == AAREN_OK) rc = AAREN_ERR_CUDA;
@@ -821,8 +834,14 @@ aaren_status_t aaren_step(const void *q, float *m, float *u, float *w, const voi
     if (!aligned(q, 16) || !aligned(k_t, 16) || !aligned(v_t, 16) || !aligned(o_t, 16))
         return AAREN_ERR_INVALID;
     if (check_state(m, u, w) != AAREN_OK) return AAREN_ERR_INVALID;
+    unsigned *status = nullptr;   // the step's only device-side report is a bounds violation
+#ifdef AAREN_CHECKED
+    if (cudaGetSymbolAddress(reinterpret_cast<void **>(&status), g_status) != cudaSuccess) return AAREN_ERR_CUDA;
+#endif
     StepParams p;
     p.q = q; p.m = m; p.u = u; p.w = w; p.k = k_t; p.v = v_t; p.o = o_t; p.n = n;
+    p.status = status;
+    p.probe = g_bounds_probe.load();
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     switch (d) {
     case 16: return dispatch_step_dtype<16>(p, dtype, st);
@@ -841,6 +860,7 @@ aaren_status_t aaren_check(void *stream)
     if (bits == 0) return AAREN_OK;
     const unsigned zero = 0;
     if (cudaMemcpyToSymbol(g_status, &zero, sizeof(zero)) != cudaSuccess) return AAREN_ERR_CUDA;
+    if (bits & STATUS_BOUNDS) return AAREN_ERR_BOUNDS;
     if (bits & STATUS_LOAD_TIMEOUT) return AAREN_ERR_LOAD_TIMEOUT;
     return AAREN_ERR_LOOKBACK_TIMEOUT;
 }
@@ -853,13 +873,14 @@ const char *aaren_status_string(int32_t status)
     case AAREN_ERR_UNSUPPORTED: return "unsupported d or dtype";
     case AAREN_ERR_CUDA: return "CUDA runtime error";
     case AAREN_ERR_LOOKBACK_TIMEOUT: return "device: cross-block carry wait gave up";
-    case AAREN_ERR_LOAD_TIMEOUT: return "device: bulk copy into shared memory did not complete";
+    case AAREN_ERR_BOUNDS: return "device (checked build): an index outside its buffer, access skipped";
+    case AAREN_ERR_LOAD_TIMEOUT: return "device: bulk copy or in-block hand-off did not complete";
     case AAREN_ERR_WORKSPACE: return "workspace too small or misaligned";
     default: return "unknown status";
     }
 }
 
-int32_t aaren_abi_version(void) { return 1; }
+int32_t aaren_abi_version(void) { return 2; }
 
 aaren_status_t aaren_debug_set_fault(int64_t never_publish_chunk, int64_t wait_limit_ns)
 {
@@ -868,10 +889,37 @@ aaren_status_t aaren_debug_set_fault(int64_t never_publish_chunk, int64_t wait_l
     return AAREN_OK;
 }
 
+aaren_status_t aaren_debug_drop_arrival(int64_t chunk)
+{
+    g_drop_chunk.store(chunk < 0 ? -1 : chunk);
+    return AAREN_OK;
+}
+
+aaren_status_t aaren_debug_bounds_probe(int64_t offset)
+{
+    g_bounds_probe.store(offset);
+    return AAREN_OK;
+}
+
+int32_t aaren_checked_build(void)
+{
+#ifdef AAREN_CHECKED
+    return 1;
+#else
+    return 0;
+#endif
+}
+
 int64_t aaren_scan_chunk_tokens(int64_t d, int32_t dtype)
 {
     if (!supported_d(d) || !supported_dtype(dtype)) return 0;
     return chunk_tokens(d, dtype);
+}
+
+int64_t aaren_backward_chunk_tokens(int64_t d, int32_t dtype)
+{
+    if (!supported_d(d) || !supported_dtype(dtype)) return 0;
+    return bwd_chunk_tokens(d, dtype);
 }
 
 }  // extern "C"

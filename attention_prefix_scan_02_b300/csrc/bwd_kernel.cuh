@@ -60,6 +60,7 @@ struct BwdParams {
     int64_t N;
     int64_t heads;
     int64_t chunks_per_head;
+    int64_t fault_chunk;   // testing: chunk that never publishes its suffix (-1 = none)
     int64_t wait_limit_ns;
 };
 
@@ -144,6 +145,9 @@ __device__ bool lookforward(const BwdParams &p, int64_t head, int64_t c, Suffix<
     const int64_t first = head * p.chunks_per_head;
     const bool owns = (L::LANES == 32 || lane < L::LANES);
     suffix_empty<E>(x);
+    // every successor slot read below lies in (first + c, first + chunks_per_head)
+    if (!AAREN_IN_BOUNDS(p.status, c >= 0 && in_range(first, p.chunks_per_head, p.heads * p.chunks_per_head)))
+        return false;
     for (int64_t j0 = c + 1; j0 < p.chunks_per_head; j0 += 32) {
         const int64_t j = j0 + lane;
         const bool has = (j < p.chunks_per_head);   // lanes past the end act as a stop
@@ -272,58 +276,6 @@ __device__ __forceinline__ Acc bwd_transpose_sum8(Acc (&x)[8], int lane)
     return y;
 }
 
-// Row dot products of a warp's 32 rows, lane = token on return: a . b_t
-// with `a` lane-owned (E values) and b_t read from shared memory.  float32
-// rows are summed in float64 (their scores reach hundreds).
-template <int D, typename Tb>
-__device__ __forceinline__ float rows_dot(const float (&a)[VLayout<D>::E], const Tb *rows, int nv,
-                                          int lane)
-{
-    using L = VLayout<D>;
-    constexpr int E = L::E;
-    const bool owns = (L::LANES == 32 || lane < L::LANES);
-    float out = 0.f;
-#pragma unroll 1
-    for (int quarter = 0; quarter < 4; ++quarter) {
-        if constexpr (sizeof(Tb) == 4) {
-            double x[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int r = quarter * 8 + i;
-                x[i] = 0.0;
-                if (owns && r < nv) {
-                    float bf[E];
-                    load_vals<E>(rows + size_t(r) * D + lane * E, bf);
-                    double acc = 0.0;
-#pragma unroll
-                    for (int e = 0; e < E; ++e) acc = fma(double(a[e]), double(bf[e]), acc);
-                    x[i] = acc;
-                }
-            }
-            const float sr = static_cast<float>(bwd_transpose_sum8<double>(x, lane));
-            if ((lane >> 3) == quarter) out = sr;
-        } else {
-            float x[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int r = quarter * 8 + i;
-                x[i] = 0.f;
-                if (owns && r < nv) {
-                    float bf[E];
-                    load_vals<E>(rows + size_t(r) * D + lane * E, bf);
-                    float acc = a[0] * bf[0];
-#pragma unroll
-                    for (int e = 1; e < E; ++e) acc = fmaf(a[e], bf[e], acc);
-                    x[i] = acc;
-                }
-            }
-            const float sr = bwd_transpose_sum8<float>(x, lane);
-            if ((lane >> 3) == quarter) out = sr;
-        }
-    }
-    return out;
-}
-
 template <int D, typename Tin, typename Tout>
 __global__ void __launch_bounds__(BwdTile<D, Tin, Tout>::WARPS * 32) k_scan_bwd(const BwdParams p)
 {
@@ -362,6 +314,8 @@ __global__ void __launch_bounds__(BwdTile<D, Tin, Tout>::WARPS * 32) k_scan_bwd(
     // tickets run from the last chunk of each head to the first, interleaved
     // over heads: every successor of a chunk holds an earlier ticket
     const int64_t ticket = *s_ticket;
+    // one block per chunk: the ticket names a chunk of the launch (uniform)
+    if (!AAREN_IN_BOUNDS(p.status, in_range(ticket, 1, p.heads * p.chunks_per_head))) return;
     const int64_t rc = ticket / p.heads;
     const int64_t head = ticket - rc * p.heads;
     const int64_t c = p.chunks_per_head - 1 - rc;
@@ -369,7 +323,15 @@ __global__ void __launch_bounds__(BwdTile<D, Tin, Tout>::WARPS * 32) k_scan_bwd(
     const int64_t t0 = c * C;
     const int nvalid = static_cast<int>(p.N - t0 < C ? p.N - t0 : C);
     const int64_t row0 = head * p.N + t0;
+    // the chunk's rows of K, V, O, dO, stats, dK and dV, the head's q and dq
+    // entries, and the chunk's workspace slot (uniform; on a violation the
+    // block reads and writes nothing and publishes nothing)
+    if (!AAREN_IN_BOUNDS(p.status, nvalid >= 1 && nvalid <= C && in_range(row0, nvalid, p.heads * p.N) &&
+                                       in_range(head, 1, p.heads) &&
+                                       in_range(chunk, 1, p.heads * p.chunks_per_head)))
+        return;
     unsigned *my_flag = p.flags + chunk;
+    const bool publish = (chunk != p.fault_chunk);   // testing hook: a suffix never published
     float *my_state = p.states + size_t(chunk) * 2 * SS;
 
     // K, O, dO rows of the chunk into shared memory (V follows into O's slot)
@@ -387,6 +349,9 @@ __global__ void __launch_bounds__(BwdTile<D, Tin, Tout>::WARPS * 32) k_scan_bwd(
     if constexpr (sizeof(Tin) == 4) {
         for (int j = tid; j < D; j += WARPS * 32)
             qs[q_slot<D, Tin>(j)] = to_f32(static_cast<const Tin *>(p.q)[head * D + j]);
+    } else {   // bfloat16 q as it is stored, for the forward's score function
+        for (int j = tid; j < D; j += WARPS * 32)
+            reinterpret_cast<Tin *>(qs)[j] = static_cast<const Tin *>(p.q)[head * D + j];
     }
     float qv[E];
     if (owns) {
@@ -407,7 +372,7 @@ __global__ void __launch_bounds__(BwdTile<D, Tin, Tout>::WARPS * 32) k_scan_bwd(
     if (__syncthreads_or(!loaded)) {
         if (tid == 0) atomicOr(p.status, STATUS_LOAD_TIMEOUT);
         wait_bar(bar, 0, p.wait_limit_ns);
-        if (warp == 0) publish_flag(my_flag, FLAG_POISON, lane);
+        if (warp == 0 && publish) publish_flag(my_flag, FLAG_POISON, lane);
         return;
     }
 
@@ -422,7 +387,8 @@ __global__ void __launch_bounds__(BwdTile<D, Tin, Tout>::WARPS * 32) k_scan_bwd(
     if constexpr (sizeof(Tin) == 4) {
         s = (lane < nv) ? dot_row<D, Tin>(Kw + size_t(lane) * D, qs, lane) : -INFINITY;
     } else {
-        s = rows_dot<D, Tin>(qv, Kw, nv, lane);
+        s = (lane < nv) ? dot_row_bf16<D>(Kw + size_t(lane) * D, reinterpret_cast<const Tin *>(qs), lane)
+                        : -INFINITY;
     }
     // g_t . o_t (both rows from shared memory), and in the same pass the R
     // part of the warp aggregate, sum_t c_t g_t with c_t = e^{lse_0 - lse_t}
@@ -504,15 +470,19 @@ __global__ void __launch_bounds__(BwdTile<D, Tin, Tout>::WARPS * 32) k_scan_bwd(
         if (c == p.chunks_per_head - 1) {
             suffix_empty<E>(x);
         } else {
-            suffix_store<D>(my_state, agg, lane);
-            publish_flag(my_flag, FLAG_AGG, lane);
+            if (publish) {
+                suffix_store<D>(my_state, agg, lane);
+                publish_flag(my_flag, FLAG_AGG, lane);
+            }
             ok = lookforward<D>(p, head, c, x, lane);
         }
         if (ok) {
             Suffix<E> inc = agg;
             suffix_append<E>(inc, x);
-            suffix_store<D>(my_state + SS, inc, lane);
-            publish_flag(my_flag, FLAG_INC, lane);
+            if (publish) {
+                suffix_store<D>(my_state + SS, inc, lane);
+                publish_flag(my_flag, FLAG_INC, lane);
+            }
             // carry into warp k = aggregates of warps k+1.. (+) the suffix after the chunk
             for (int k = WARPS - 1; k >= 0; --k) {
                 suffix_store<D>(cst + k * SS, x, lane);
@@ -526,7 +496,7 @@ __global__ void __launch_bounds__(BwdTile<D, Tin, Tout>::WARPS * 32) k_scan_bwd(
                 atomicOr(p.status, STATUS_LOOKBACK_TIMEOUT);
                 *s_abort = 1;
             }
-            publish_flag(my_flag, FLAG_POISON, lane);
+            if (publish) publish_flag(my_flag, FLAG_POISON, lane);
         }
     }
     __syncthreads();

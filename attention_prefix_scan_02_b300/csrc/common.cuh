@@ -11,7 +11,32 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr unsigned kFull = 0xffffffffu;
 
 // Bits of the per-device status word (reported by aaren_check).
-enum : unsigned { STATUS_LOOKBACK_TIMEOUT = 1u, STATUS_LOAD_TIMEOUT = 2u };
+enum : unsigned { STATUS_LOOKBACK_TIMEOUT = 1u, STATUS_LOAD_TIMEOUT = 2u, STATUS_BOUNDS = 4u };
+
+// Checked build.  Compiled with -DAAREN_CHECKED, every kernel tests each
+// extent it computes (rows of a global tensor, a workspace slot, a bulk copy,
+// a shared-memory stage) against its buffer before the access; a violation
+// ORs STATUS_BOUNDS into the device status word (reported by aaren_check as
+// AAREN_ERR_BOUNDS) and the access is skipped.  In the regular build
+// AAREN_IN_BOUNDS is the constant true and the tested expression is never
+// evaluated, so the regular kernels carry none of it.
+#ifdef AAREN_CHECKED
+#define AAREN_IN_BOUNDS(status, cond) (::aaren::bounds_ok((status), (cond)))
+#else
+#define AAREN_IN_BOUNDS(status, cond) (true)
+#endif
+
+__device__ __forceinline__ bool bounds_ok(unsigned *status, bool ok)
+{
+    if (!ok) atomicOr(status, STATUS_BOUNDS);
+    return ok;
+}
+
+// [first, first + count) lies inside [0, extent).
+__device__ __forceinline__ bool in_range(int64_t first, int64_t count, int64_t extent)
+{
+    return first >= 0 && count >= 0 && first <= extent && count <= extent - first;
+}
 
 // How value dimensions are spread over a warp: LANES lanes own E consecutive
 // dims each (d = 16 leaves lanes 16..31 without dims).
@@ -32,6 +57,51 @@ __device__ __forceinline__ unsigned f32x2_to_bf16x2(float lo, float hi)
 {
     __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);   // round to nearest even
     return *reinterpret_cast<unsigned *>(&h);
+}
+
+// Packed float32 pairs for the sm_100 family's two-wide float32 FMA and
+// multiply (one instruction for two lanes' worth of work): .x in the low
+// word.  Rounding is that of the scalar fmaf / multiply, element by element.
+__device__ __forceinline__ uint64_t pack2(float lo, float hi)
+{
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+
+__device__ __forceinline__ void unpack2(uint64_t x, float &lo, float &hi)
+{
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(x));
+}
+
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c)
+{
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
+__device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b)
+{
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+// Two bfloat16 products accumulated in float32 with the sm_100 family's
+// mixed-precision FMA: lo += a.lo * b.lo, hi += a.hi * b.hi for bfloat16 pairs
+// a, b (the element at the lower address in the low half).  A product of two
+// bfloat16 values is exact in float32, so each step rounds once, as fmaf
+// on the widened values would.
+__device__ __forceinline__ void fma_bf16x2(float &lo, float &hi, unsigned a, unsigned b)
+{
+    asm("{\n\t.reg .b16 al, ah, bl, bh;\n\t"
+        "mov.b32 {al, ah}, %2;\n\t"
+        "mov.b32 {bl, bh}, %3;\n\t"
+        "fma.rn.f32.bf16 %0, al, bl, %0;\n\t"
+        "fma.rn.f32.bf16 %1, ah, bh, %1;\n\t}"
+        : "+f"(lo), "+f"(hi)
+        : "r"(a), "r"(b));
 }
 
 __device__ __forceinline__ float to_f32(float x) { return x; }

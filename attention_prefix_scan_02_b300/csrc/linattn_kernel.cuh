@@ -94,6 +94,8 @@ struct Params {
     double inv_2M;              // position * inv_2M = angle / pi
     unsigned *status;
     int64_t wait_limit_ns;
+    int64_t drop_chunk;         // testing: chunk (of CTA 0) whose weighted keys are never
+                                // announced, so the MMA warp's wait gives up (-1 = none)
 };
 
 struct Bars {
@@ -104,9 +106,11 @@ struct Bars {
     uint64_t aready;              // A in tensor memory (both row warpgroups): MMA2
     uint64_t pfull, dsfull, ofull;   // MMA completion (commit)
     uint64_t tfree;               // inter / intra read (both row warpgroups)
+    uint64_t drain;               // after a give-up: every MMA issued so far has completed
     uint32_t tmem;
     int abort;
 };
+static_assert(sizeof(Bars) <= 128, "the barriers' shared-memory slot is 128 bytes");
 
 __device__ __forceinline__ uint32_t relu_bf16x2(uint32_t w)
 {
@@ -244,6 +248,7 @@ k_linattn(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtens
         ptx::mbar_init(&b.kw, 1); ptx::mbar_init(&b.sready, 1); ptx::mbar_init(&b.aready, 2);
         ptx::mbar_init(&b.pfull, 1); ptx::mbar_init(&b.dsfull, 1); ptx::mbar_init(&b.ofull, 1);
         ptx::mbar_init(&b.tfree, 2);
+        ptx::mbar_init(&b.drain, 1);
         b.abort = 0;
         ptx::fence_barrier_init();
     }
@@ -277,11 +282,16 @@ k_linattn(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtens
                 if (!la_wait(b, &b.empty[s], static_cast<unsigned>(((g >> 1) & 1) ^ 1), p)) break;
                 const int64_t h = blockIdx.x + (g / nc) * gridDim.x, c = g % nc;
                 uint8_t *st = sm + OFF_STAGE + s * 3 * kTile;
-                ptx::mbar_arrive_expect_tx(&b.full[s], 3 * kTile);
                 const int y = static_cast<int>(c * C), z = static_cast<int>(h);
-                tc::tma_load_3d(st, &tq, 0, y, z, &b.full[s]);
-                tc::tma_load_3d(st + kTile, &tk, 0, y, z, &b.full[s]);
-                tc::tma_load_3d(st + 2 * kTile, &tv, 0, y, z, &b.full[s]);
+                // the tile's first row and its head lie inside the tensors
+                if (AAREN_IN_BOUNDS(p.status, in_range(h, 1, p.BH) && in_range(c * C, 1, p.N))) {
+                    ptx::mbar_arrive_expect_tx(&b.full[s], 3 * kTile);
+                    tc::tma_load_3d(st, &tq, 0, y, z, &b.full[s]);
+                    tc::tma_load_3d(st + kTile, &tk, 0, y, z, &b.full[s]);
+                    tc::tma_load_3d(st + 2 * kTile, &tv, 0, y, z, &b.full[s]);
+                } else {
+                    ptx::mbar_arrive(&b.full[s]);   // no copy: the fill completes at once
+                }
             }
             // let copies still in flight land before the CTA can exit
             for (int64_t k = g - 2 > 0 ? g - 2 : 0; k < g; ++k)
@@ -292,8 +302,7 @@ k_linattn(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtens
         if (lane == 0) {
             const uint32_t kw0 = tc::saddr(sm + OFF_KW), s0 = tc::saddr(sm + OFF_S);
             const uint32_t ones = tc::saddr(sm + OFF_ONES);
-            uint64_t *last = nullptr;
-            unsigned last_par = 0;
+            const uint64_t *last = nullptr;   // the latest commit (null: no MMA issued yet)
             for (int64_t g = 0; g < total; ++g) {
                 const int s = static_cast<int>(g & 1);
                 const unsigned par = static_cast<unsigned>(g & 1), prev = par ^ 1u;
@@ -308,7 +317,7 @@ k_linattn(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtens
                     tc::mma_ss(tmem + COL_P, tc::sdesc(q0 + kk * 32, 16, 1024), tc::sdesc(k0 + kk * 32, 16, 1024),
                                ID_QK, kk > 0);
                 tc::commit(&b.pfull);
-                last = &b.pfull; last_par = par;
+                last = &b.pfull;
                 // MMA4 (state update), MMA3 (inter) and MMA2 (intra) as their
                 // operands come ready, in whatever order that is; the output
                 // barrier covers MMA3 and MMA2, MMA4 has its own
@@ -325,7 +334,7 @@ k_linattn(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtens
                                 tc::mma_ss(tmem + COL_DS, tc::sdesc(kw0 + hl * 2 * kTile + kk * 2048, kTile, 1024),
                                            tc::sdesc(v0 + kk * 2048, ones - v0, 1024), ID_KV, hl > 0 || kk > 0);
                         tc::commit(&b.dsfull);
-                        last = &b.dsfull; last_par = par;
+                        last = &b.dsfull;
                         d4 = any = true;
                     }
                     if (!tf) tf = ptx::mbar_test_wait(&b.tfree, prev);   // inter / intra of the previous chunk read
@@ -352,7 +361,7 @@ k_linattn(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtens
                     }
                     if (d2 && d3 && !dO) {   // exactly one output commit per chunk
                         tc::commit(&b.ofull);
-                        last = &b.ofull; last_par = par;
+                        last = &b.ofull;
                         dO = true;
                     }
                     if (!any) {
@@ -370,8 +379,14 @@ k_linattn(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtens
                     break;
                 }
             }
-            if (aborted(b) && last != nullptr)   // gave up: let MMAs still in flight finish
-                wait_bar(last, last_par, p.wait_limit_ns);
+            // gave up: let every MMA still in flight finish before tensor
+            // memory is freed.  A commit covers all earlier MMAs of this
+            // thread, including any issued after the last per-chunk commit
+            // (a give-up inside the poll loop can leave MMA3 or MMA2 without one).
+            if (aborted(b) && last != nullptr) {
+                tc::commit(&b.drain);
+                wait_bar(&b.drain, 0, p.wait_limit_ns);
+            }
         }
     } else if (warp >= 4 && warp < 12) {
         // ---------------- row warpgroups: token rows, half hf of the columns each ----------------
@@ -458,7 +473,8 @@ k_linattn(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtens
                 for (int t = 0; t < 32; ++t)
                     o[t] = (__uint_as_float(x[t]) + cs * __uint_as_float(ic[t]) + sn * __uint_as_float(is[t])) * r;
                 const int64_t row = c * C + i;
-                if (row < p.N) store_row32(reinterpret_cast<Tout *>(p.O) + (h * p.N + row) * D + b0, o);
+                if (row < p.N && AAREN_IN_BOUNDS(p.status, in_range(h * p.N + row, 1, p.BH * p.N)))
+                    store_row32(reinterpret_cast<Tout *>(p.O) + (h * p.N + row) * D + b0, o);
             }
             tc::fence_before();
             ptx::named_bar_sync(nb, 128);
@@ -479,7 +495,7 @@ k_linattn(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtens
         float z = 0.f;
         // the state a head starts from: the caller's, or zero
         auto load_start = [&](int64_t h) {
-            if (p.S_in != nullptr) {
+            if (p.S_in != nullptr && AAREN_IN_BOUNDS(p.status, in_range(h, 1, p.BH))) {
                 const float4 *src = reinterpret_cast<const float4 *>(p.S_in + ((h * 2 + half) * 64 + k) * 64);
 #pragma unroll
                 for (int q4 = 0; q4 < 16; ++q4) {
@@ -554,7 +570,7 @@ k_linattn(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtens
             tc::fence_async_smem();
             tc::fence_before();
             ptx::named_bar_sync(3, 128);
-            if (r == 0) ptx::mbar_arrive(&b.kw);
+            if (r == 0 && !(blockIdx.x == 0 && g == p.drop_chunk)) ptx::mbar_arrive(&b.kw);
 
             // ---- dS, dz of this chunk; then the stage is no longer read here or by MMA4 ----
             la_wait(b, &b.dsfull, par, p);
@@ -574,7 +590,7 @@ k_linattn(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtens
             }
             if (r == 0) ptx::mbar_arrive(&b.empty[s]);
             if (c == nc - 1) {   // end of a head: its final state, then the next head's start
-                if (p.S_out != nullptr && !aborted(b)) {
+                if (p.S_out != nullptr && !aborted(b) && AAREN_IN_BOUNDS(p.status, in_range(h, 1, p.BH))) {
                     float4 *dst = reinterpret_cast<float4 *>(p.S_out + ((h * 2 + half) * 64 + k) * 64);
 #pragma unroll
                     for (int q4 = 0; q4 < 16; ++q4)

@@ -59,6 +59,8 @@ struct ReduceParams {
     int64_t heads;
     int64_t P;             // parts per head
     int64_t seg;           // tokens per part (a multiple of kReduceRows)
+    int64_t part_slots;    // part states the workspace holds (checked build)
+    unsigned *status;      // device status word (checked build)
 };
 
 // Streaming loads (read once: evict first).
@@ -291,6 +293,12 @@ __global__ void __launch_bounds__(kReduceWarps * 32) k_scan_reduce(const ReduceP
     const bool owns = (L::LANES == 32 || lane < L::LANES);
     const int64_t r0 = part * p.seg;
     const int64_t r1 = (r0 + p.seg < p.N) ? r0 + p.seg : p.N;   // r0 may be >= r1 (empty part)
+    // the part's rows of K and V, the head's q and counter, the part's slot
+    // and the head's parts in the workspace (uniform per warp)
+    if (!AAREN_IN_BOUNDS(p.status, in_range(head, 1, p.heads) && in_range(gw, 1, p.part_slots) &&
+                                       in_range(head * p.P, p.P, p.part_slots) &&
+                                       (r0 >= r1 || in_range(head * p.N + r0, r1 - r0, p.heads * p.N))))
+        return;
 
     float qv[E];
     if (owns) {

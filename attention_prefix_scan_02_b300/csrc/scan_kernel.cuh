@@ -68,6 +68,8 @@ struct ScanParams {
     int64_t heads;           // B * H
     int64_t chunks_per_head;
     int64_t fault_chunk;     // testing: chunk that never publishes (-1 = none)
+    int64_t drop_chunk;      // testing: chunk whose compute warp 0 never reports its
+                             // aggregate to its group (persistent kernel; -1 = none)
     int64_t wait_limit_ns;
 };
 
@@ -173,6 +175,34 @@ __device__ __forceinline__ float dot_row(const Tin *krow, const float *qs, int l
     }
 }
 
+// s = q . k for one bfloat16 key row in shared memory, lane = token, q in
+// shared memory as bfloat16 [D].  Both operands go straight into the float32
+// accumulation (mixed-precision FMA, exact products), in four chains.  The
+// row and q are read in 16-byte pieces starting at piece `lane` (mod the
+// piece count), so the eight rows a quarter-warp reads at a time sit in
+// distinct banks for d >= 64.  Every kernel that scores bfloat16 keys this
+// way gets bitwise the same score for the same token (lane = token mod 32 in
+// all of them).
+template <int D>
+__device__ __forceinline__ float dot_row_bf16(const __nv_bfloat16 *krow, const __nv_bfloat16 *qsm, int lane)
+{
+    constexpr int NCH = D / 8;   // 16-byte pieces per row (power of two)
+    const uint4 *kr = reinterpret_cast<const uint4 *>(krow);
+    const uint4 *qr = reinterpret_cast<const uint4 *>(qsm);
+    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+    for (int i = 0; i < NCH; ++i) {
+        const int ch = (i + lane) & (NCH - 1);
+        const uint4 k = kr[ch];
+        const uint4 q = qr[ch];
+        fma_bf16x2(a0, a1, q.x, k.x);
+        fma_bf16x2(a2, a3, q.y, k.y);
+        fma_bf16x2(a0, a1, q.z, k.z);
+        fma_bf16x2(a2, a3, q.w, k.w);
+    }
+    return (a0 + a1) + (a2 + a3);
+}
+
 // Bounded wait on an mbarrier phase; false when it gave up.
 __device__ __forceinline__ bool wait_bar(uint64_t *bar, unsigned parity, int64_t limit_ns)
 {
@@ -261,6 +291,9 @@ __device__ bool lookback(const ScanParams &p, int64_t head, int64_t c, float &xm
     constexpr int SS = StateLayout<D>::SS;
     const int64_t first = head * p.chunks_per_head;   // chunk 0 of this head
     const bool owns = (L::LANES == 32 || lane < L::LANES);
+    // every predecessor slot read below lies in [first, first + c), inside the workspace
+    if (!AAREN_IN_BOUNDS(p.status, c <= p.chunks_per_head && in_range(first, c, p.heads * p.chunks_per_head)))
+        return false;
     for (int64_t j0 = c - 1; j0 >= 0; j0 -= 32) {
         const int64_t j = j0 - lane;
         const bool has = (j >= 0);                       // lanes before chunk 0 act as a stop
@@ -442,6 +475,8 @@ __global__ void __launch_bounds__(WARPS * 32)
     // in flight spread over all heads and their carries progress in parallel;
     // within a head, chunk c - 1 always has an earlier ticket than chunk c
     const int64_t ticket = *s_chunk;
+    // one block per chunk: the ticket names a chunk of the launch (uniform)
+    if (!AAREN_IN_BOUNDS(p.status, in_range(ticket, 1, p.heads * p.chunks_per_head))) return;
     const int64_t c = ticket / p.heads;
     const int64_t head = ticket - c * p.heads;
     const int64_t chunk = head * p.chunks_per_head + c;   // workspace slot
@@ -451,14 +486,26 @@ __global__ void __launch_bounds__(WARPS * 32)
     const bool publish = (chunk != p.fault_chunk);
     unsigned *my_flag = p.flags + chunk;
     float *my_state = p.states + size_t(chunk) * 2 * SS;
+    // the chunk's rows of K, V, O (and stats) and its slot of the workspace
+    const bool rows_ok = AAREN_IN_BOUNDS(p.status, nvalid >= 1 && nvalid <= C && in_range(row0, nvalid, p.heads * p.N) &&
+                                                       in_range(chunk, 1, p.heads * p.chunks_per_head) &&
+                                                       in_range(head, 1, p.heads));
 
     // 1. K and V rows of the chunk into shared memory (one bulk copy each)
     if (tid == 0) {
-        const unsigned bytes = static_cast<unsigned>(nvalid) * D * sizeof(Tin);
-        ptx::mbar_arrive_expect_tx(bar, 2 * bytes);
-        const uint64_t pol = ptx::policy_evict_first();
-        ptx::bulk_g2s(Ks, static_cast<const Tin *>(p.K) + row0 * D, bytes, bar, pol);
-        ptx::bulk_g2s(Vs, static_cast<const Tin *>(p.V) + row0 * D, bytes, bar, pol);
+        if (rows_ok) {
+            const unsigned bytes = static_cast<unsigned>(nvalid) * D * sizeof(Tin);
+            ptx::mbar_arrive_expect_tx(bar, 2 * bytes);
+            const uint64_t pol = ptx::policy_evict_first();
+            ptx::bulk_g2s(Ks, static_cast<const Tin *>(p.K) + row0 * D, bytes, bar, pol);
+            ptx::bulk_g2s(Vs, static_cast<const Tin *>(p.V) + row0 * D, bytes, bar, pol);
+        } else {
+            ptx::mbar_arrive(bar);   // no copy: the phase completes at once
+        }
+    }
+    if (!rows_ok) {   // uniform: nothing of this chunk is read or written
+        wait_bar(bar, 0, p.wait_limit_ns);
+        return;
     }
     for (int j = tid; j < D; j += WARPS * 32)
         qs[q_slot<D, Tin>(j)] = to_f32(static_cast<const Tin *>(p.q)[head * D + j]);

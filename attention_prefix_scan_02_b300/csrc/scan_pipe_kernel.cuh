@@ -174,20 +174,7 @@ __device__ __forceinline__ void lds_row(const __nv_bfloat16 *p, RawRow<E> &r)
     }
 }
 
-template <int E>
-__device__ __forceinline__ void unpack_row(const RawRow<E> &r, float (&f)[E])
-{
-    if constexpr (E == 4) {
-        bf16x2_to_f32(r.w[0], f[0], f[1]);
-        bf16x2_to_f32(r.w[1], f[2], f[3]);
-    } else if constexpr (E == 2) {
-        bf16x2_to_f32(r.w[0], f[0], f[1]);
-    } else {
-        f[0] = __uint_as_float(r.w[0] << 16);
-    }
-}
-
-// unpack_row with the zero bits taken from a register z (always 0) that the
+// The bfloat16 row widened to float32, with the zero bits taken from a register z (always 0) that the
 // caller loads just before the row is used.  The dependency keeps the
 // compiler from converting all 32 register-held rows at once, long before
 // they are needed (which would triple the registers V occupies).
@@ -203,28 +190,6 @@ __device__ __forceinline__ void unpack_row_late(const RawRow<E> &r, unsigned z, 
     }
 #pragma unroll
     for (int e = 0; e < E; ++e) f[e] = __uint_as_float(a[e]);
-}
-
-// x[i] holds this lane's share of row i's dot product (i < 8).  Returns, on
-// every lane, the full sum over the 32 lanes for row (lane & 7): a butterfly
-// that halves the rows each lane keeps at every exchange (4 + 2 + 1
-// shuffles), then two exchanges that add up the four groups of eight lanes.
-__device__ __forceinline__ float transpose_sum8(float (&x)[8], int lane)
-{
-#pragma unroll
-    for (int h = 4; h >= 1; h >>= 1) {
-        const bool upper = (lane & h) != 0;
-#pragma unroll
-        for (int i = 0; i < h; ++i) {
-            const float send = upper ? x[i] : x[i + h];
-            const float keep = upper ? x[i + h] : x[i];
-            x[i] = keep + __shfl_xor_sync(kFull, send, h);
-        }
-    }
-    float y = x[0];
-    y += __shfl_xor_sync(kFull, y, 8);
-    y += __shfl_xor_sync(kFull, y, 16);
-    return y;
 }
 
 // Non-blocking test of an mbarrier phase by a whole warp: true only when
@@ -372,13 +337,20 @@ __global__ void __launch_bounds__(PipeTile<D, GROUPS, STAGES, Tin>::THREADS, 1)
                         const unsigned bytes = static_cast<unsigned>(nvalid) * D * sizeof(Tin);
                         const int64_t row0 = head * p.N + t0;
                         unsigned char *stage = smem + size_t(st) * T::stage_bytes;
-                        ptx::mbar_arrive_expect_tx(full + st, 2 * bytes + unsigned(T::q_bytes));
-                        ptx::bulk_g2s(stage, static_cast<const Tin *>(p.K) + row0 * D, bytes, full + st,
-                                      pol);
-                        ptx::bulk_g2s(stage + T::st_v, static_cast<const Tin *>(p.V) + row0 * D, bytes,
-                                      full + st, pol);
-                        ptx::bulk_g2s(stage + T::st_q, static_cast<const Tin *>(p.q) + head * D,
-                                      unsigned(T::q_bytes), full + st, pol);
+                        // a stage of the pool, the chunk's rows of K and V and the head's q
+                        if (AAREN_IN_BOUNDS(p.status, st < STAGES && nvalid >= 1 && nvalid <= C &&
+                                                          in_range(row0, nvalid, p.heads * p.N) &&
+                                                          in_range(head, 1, p.heads))) {
+                            ptx::mbar_arrive_expect_tx(full + st, 2 * bytes + unsigned(T::q_bytes));
+                            ptx::bulk_g2s(stage, static_cast<const Tin *>(p.K) + row0 * D, bytes, full + st,
+                                          pol);
+                            ptx::bulk_g2s(stage + T::st_v, static_cast<const Tin *>(p.V) + row0 * D, bytes,
+                                          full + st, pol);
+                            ptx::bulk_g2s(stage + T::st_q, static_cast<const Tin *>(p.q) + head * D,
+                                          unsigned(T::q_bytes), full + st, pol);
+                        } else if (st < STAGES) {
+                            ptx::mbar_arrive(full + st);   // no copy: the fill completes at once
+                        }
                     }
                     ptx::mbar_arrive(metab);
                 }
@@ -402,7 +374,10 @@ __global__ void __launch_bounds__(PipeTile<D, GROUPS, STAGES, Tin>::THREADS, 1)
             const int64_t c = t / p.heads;
             const int64_t head = t - c * p.heads;
             const int64_t chunk = head * p.chunks_per_head + c;   // workspace slot
-            const bool publish = (chunk != p.fault_chunk);
+            // the chunk's workspace slot and the head's state rows
+            const bool slot_ok = AAREN_IN_BOUNDS(p.status, in_range(chunk, 1, p.heads * p.chunks_per_head) &&
+                                                               in_range(head, 1, p.heads));
+            const bool publish = (chunk != p.fault_chunk) && slot_ok;
             unsigned *my_flag = p.flags + chunk;
             float *my_state = p.states + size_t(chunk) * 2 * SS;
 
@@ -411,13 +386,13 @@ __global__ void __launch_bounds__(PipeTile<D, GROUPS, STAGES, Tin>::THREADS, 1)
             for (int e = 0; e < E; ++e) xu[e] = 0.f;
             bool lb_ok = true;
             if (c == 0) {
-                if (p.m_in != nullptr) {
+                if (p.m_in != nullptr && slot_ok) {
                     xm = p.m_in[head];
                     xw = p.w_in[head];
                     if (owns) load_vals<E>(p.u_in + head * D + lane * E, xu);
                 }
             } else {
-                lb_ok = lookback<D, kPipeFoldBatch>(p, head, c, xm, xu, xw, lane);
+                lb_ok = slot_ok && lookback<D, kPipeFoldBatch>(p, head, c, xm, xu, xw, lane);
             }
             // chunk aggregate from the four warp aggregates
             if (!wait_bar(aggb, par, group_limit)) {
@@ -465,7 +440,7 @@ __global__ void __launch_bounds__(PipeTile<D, GROUPS, STAGES, Tin>::THREADS, 1)
                 }
             } else {
                 if (lane == 0) {
-                    atomicOr(p.status, STATUS_LOOKBACK_TIMEOUT);
+                    if (slot_ok) atomicOr(p.status, STATUS_LOOKBACK_TIMEOUT);
                     *fail = 1;
                 }
                 __syncwarp();
@@ -494,6 +469,7 @@ __global__ void __launch_bounds__(PipeTile<D, GROUPS, STAGES, Tin>::THREADS, 1)
         const int st_word = *meta_s;
         const int st = st_word & 0xff;
         const unsigned fill_par = static_cast<unsigned>(st_word >> 8) & 1u;
+        if (!AAREN_IN_BOUNDS(p.status, st < STAGES)) break;   // a stage of the pool
         if (!compute_wait(full + st, fill_par, group_limit)) {
             if (lane == 0) atomicOr(p.status, STATUS_LOAD_TIMEOUT);
             break;
@@ -505,50 +481,26 @@ __global__ void __launch_bounds__(PipeTile<D, GROUPS, STAGES, Tin>::THREADS, 1)
         const int nvalid = static_cast<int>(p.N - t0 < C ? p.N - t0 : C);
         int nv = nvalid - wg * 32;                            // valid rows of this warp
         nv = nv < 0 ? 0 : (nv > 32 ? 32 : nv);
+        // this warp's rows of O and stats, and the chunk's workspace slot
+        // (on a violation the warp computes but writes nothing)
+        // (a warp past the end of a ragged last chunk has no rows: nv = 0)
+        const bool rows_ok = AAREN_IN_BOUNDS(
+            p.status, (nv == 0 || in_range(head * p.N + t0 + wg * 32, nv, p.heads * p.N)) &&
+                          in_range(head * p.chunks_per_head + c, 1, p.heads * p.chunks_per_head));
 
-        float qv[E];
-        if (owns) {
-            load_vals<E>(reinterpret_cast<const Tin *>(stage + T::st_q) + lane * E, qv);
-        } else {
-#pragma unroll
-            for (int e = 0; e < E; ++e) qv[e] = 0.f;
-        }
-
-        // 1. scores (lane = dims, then transposed to lane = token).  The row
-        //    loops that need no register-held V stay rolled: the code of all
-        //    warps must fit the SM's instruction cache.
-        const Tin *Kw = reinterpret_cast<const Tin *>(stage) + size_t(wg) * 32 * D + lane * E;
+        // 1. scores, lane = token.  float32 keys: the compensated dot product
+        //    of the one-chunk-per-block kernel and the backward pass;
+        //    bfloat16 keys: the mixed-precision dot product the backward pass
+        //    also uses (the same functions, so every kernel sees bitwise the
+        //    same score).
         const Tin *Vw = reinterpret_cast<const Tin *>(stage + T::st_v) + size_t(wg) * 32 * D + lane * E;
         float s = -INFINITY;
-        if constexpr (sizeof(Tin) == 4) {
-            // float32 keys: lane = token, the compensated dot product of the
-            // one-chunk-per-block kernel and the backward pass (the same
-            // function, so every kernel sees bitwise the same score)
-            const float *qs = reinterpret_cast<const float *>(stage + T::st_q);
-            if (lane < nv)
-                s = dot_row<D, Tin>(reinterpret_cast<const Tin *>(stage) + size_t(wg * 32 + lane) * D, qs, lane);
-        } else {
-#pragma unroll 1
-        for (int quarter = 0; quarter < 4; ++quarter) {
-            float x[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int r = quarter * 8 + i;
-                x[i] = 0.f;
-                if (owns && r < nv) {
-                    RawRow<E> kr;
-                    lds_row<E>(Kw + size_t(r) * D, kr);
-                    float kf[E];
-                    unpack_row<E>(kr, kf);
-                    float acc = qv[0] * kf[0];
-#pragma unroll
-                    for (int e = 1; e < E; ++e) acc = fmaf(qv[e], kf[e], acc);
-                    x[i] = acc;
-                }
-            }
-            const float sr = transpose_sum8(x, lane);
-            if ((lane >> 3) == quarter) s = sr;
-        }
+        if (lane < nv) {
+            const Tin *krow = reinterpret_cast<const Tin *>(stage) + size_t(wg * 32 + lane) * D;
+            if constexpr (sizeof(Tin) == 4)
+                s = dot_row<D, Tin>(krow, reinterpret_cast<const float *>(stage + T::st_q), lane);
+            else
+                s = dot_row_bf16<D>(krow, reinterpret_cast<const __nv_bfloat16 *>(stage + T::st_q), lane);
         }
         if (lane >= nv) s = -INFINITY;
 
@@ -567,21 +519,39 @@ __global__ void __launch_bounds__(PipeTile<D, GROUPS, STAGES, Tin>::THREADS, 1)
         const float b = (s == -INFINITY) ? 0.f : exp_rel(s, mw);
         const float ww = warp_sum(b);
         {
-            float u[E];
+            // u_w = sum_r b_r v_r over the warp's rows, two dims per packed FMA
+            constexpr int P2 = (E + 1) / 2;
+            uint64_t u2[P2];
 #pragma unroll
-            for (int e = 0; e < E; ++e) u[e] = 0.f;
+            for (int k = 0; k < P2; ++k) u2[k] = 0ull;
+            float u1 = 0.f;   // d = 16: one dim per lane
 #pragma unroll
             for (int r = 0; r < 32; ++r) {
                 const float br = __shfl_sync(kFull, b, r);
                 float v[E];
                 unpack_row_late<E>(vr[r], 0u, v);
+                if constexpr (E >= 2) {
+                    const uint64_t bb = pack2(br, br);
 #pragma unroll
-                for (int e = 0; e < E; ++e) u[e] = fmaf(br, v[e], u[e]);
+                    for (int k = 0; k < E / 2; ++k) u2[k] = ffma2(bb, pack2(v[2 * k], v[2 * k + 1]), u2[k]);
+                } else {
+                    u1 = fmaf(br, v[0], u1);
+                }
+            }
+            float u[E];
+            if constexpr (E >= 2) {
+#pragma unroll
+                for (int k = 0; k < E / 2; ++k) unpack2(u2[k], u[2 * k], u[2 * k + 1]);
+            } else {
+                u[0] = u1;
             }
             write_state<D>(wst + par * WS + wg * SS, mw, u, ww, lane);
         }
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(aggb);
+        // (testing hook: warp 0 of one chunk withholds its arrival, so the
+        // group's waits on the aggregates give up)
+        if (lane == 0 && !(wg == 0 && head * p.chunks_per_head + c == p.drop_chunk))
+            ptx::mbar_arrive(aggb);
 
         // then hand the stage back to the pool (compute warp 0, once all four
         // warps are done with it)
@@ -608,7 +578,7 @@ __global__ void __launch_bounds__(PipeTile<D, GROUPS, STAGES, Tin>::THREADS, 1)
         //    may already have published the inclusive prefix, which wins.
         if (wg == (kPipeComputeWarps > 1 ? 1 : 0) && c > 0) {
             const int64_t chunk = head * p.chunks_per_head + c;
-            if (chunk != p.fault_chunk && compute_wait(aggb, par, group_limit)) {
+            if (chunk != p.fault_chunk && rows_ok && compute_wait(aggb, par, group_limit)) {
                 float am, aw, au[E];
                 chunk_aggregate<D>(wst + par * WS, am, au, aw, lane);
                 write_state<D>(p.states + size_t(chunk) * 2 * SS, am, au, aw, lane);
@@ -624,7 +594,7 @@ __global__ void __launch_bounds__(PipeTile<D, GROUPS, STAGES, Tin>::THREADS, 1)
         if (*fail) continue;
 
         // 5. rescan from the carry, V from registers, and write O
-        if (nv > 0) {
+        if (nv > 0 && rows_ok) {
             float rm, rw, u[E];
             read_state_smem<D>(cst + wg * SS, rm, u, rw, lane);
             // scalar recurrences across lanes (lane = token)
@@ -660,6 +630,13 @@ __global__ void __launch_bounds__(PipeTile<D, GROUPS, STAGES, Tin>::THREADS, 1)
             // stays in registers under static names), the blocks are not, and
             // the register-held rows shift down by one block after each (a
             // few moves, for a loop body that fits the instruction cache).
+            // u in packed pairs (two dims per FMA / multiply; d = 16 keeps one)
+            constexpr int P2 = (E + 1) / 2;
+            uint64_t u2[P2];
+            if constexpr (E >= 2) {
+#pragma unroll
+                for (int k = 0; k < E / 2; ++k) u2[k] = pack2(u[2 * k], u[2 * k + 1]);
+            }
 #pragma unroll 1
             for (int rb = 0; rb < nv; rb += kRescanBlock) {
 #pragma unroll
@@ -669,14 +646,22 @@ __global__ void __launch_bounds__(PipeTile<D, GROUPS, STAGES, Tin>::THREADS, 1)
                     const float4 k = cf[r];
                     float v[E], o[E];
                     unpack_row_late<E>(vr[i], __float_as_uint(k.w), v);
-                    if (k.x != 1.0f) {
+                    if constexpr (E >= 2) {
+                        if (k.x != 1.0f) {
+                            const uint64_t aa = pack2(k.x, k.x);
 #pragma unroll
-                        for (int e = 0; e < E; ++e) u[e] *= k.x;
-                    }
+                            for (int j = 0; j < E / 2; ++j) u2[j] = fmul2(u2[j], aa);
+                        }
+                        const uint64_t bb = pack2(k.y, k.y), rr = pack2(k.z, k.z);
 #pragma unroll
-                    for (int e = 0; e < E; ++e) {
-                        u[e] = fmaf(k.y, v[e], u[e]);
-                        o[e] = u[e] * k.z;
+                        for (int j = 0; j < E / 2; ++j) {
+                            u2[j] = ffma2(bb, pack2(v[2 * j], v[2 * j + 1]), u2[j]);
+                            unpack2(fmul2(u2[j], rr), o[2 * j], o[2 * j + 1]);
+                        }
+                    } else {
+                        if (k.x != 1.0f) u[0] *= k.x;
+                        u[0] = fmaf(k.y, v[0], u[0]);
+                        o[0] = u[0] * k.z;
                     }
                     if (owns) store_vals<E>(orow + size_t(r) * D, o);
                 }

@@ -23,6 +23,9 @@ struct StepParams {
     const void *v;
     void *o;
     int64_t n;
+    unsigned *status;     // device status word (checked build)
+    int64_t probe;        // testing, checked build: added to the stream index the
+                          // bounds check tests (never to an address)
 };
 
 template <int D, typename Tin, typename Tout>
@@ -33,6 +36,8 @@ __global__ void __launch_bounds__(256) k_step(const StepParams p)
     const int lane = threadIdx.x & 31;
     const int64_t i = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     if (i >= p.n) return;   // uniform per warp
+    // every access below is row i of an [n, ...] tensor
+    if (!AAREN_IN_BOUNDS(p.status, in_range(i + p.probe, 1, p.n))) return;
     const bool owns = (L::LANES == 32 || lane < L::LANES);
     const size_t off = size_t(i) * D + lane * E;
 

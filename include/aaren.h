@@ -60,9 +60,12 @@ typedef enum {
     AAREN_ERR_UNSUPPORTED = 2,      /* d or dtype not built */
     AAREN_ERR_CUDA = 3,             /* a CUDA runtime call failed */
     AAREN_ERR_LOOKBACK_TIMEOUT = 4, /* device: a cross-block carry wait gave up */
-    AAREN_ERR_LOAD_TIMEOUT = 5,     /* device: a bulk copy into shared memory
+    AAREN_ERR_BOUNDS = 5,           /* device, checked build only: an index fell
+                                       outside its buffer; the access was skipped */
+    AAREN_ERR_LOAD_TIMEOUT = 6,     /* device: a bulk copy into shared memory, or
+                                       a hand-off between the warps of a block,
                                        did not complete in time */
-    AAREN_ERR_WORKSPACE = 6         /* caller workspace too small or misaligned */
+    AAREN_ERR_WORKSPACE = 7         /* caller workspace too small or misaligned */
 } aaren_status_t;
 
 typedef enum {
@@ -286,7 +289,8 @@ aaren_status_t aaren_linattn_forward(const void *Q, const void *K, const void *V
  * aaren_check -- synchronise `stream`, then report and clear the device
  * status word of the current device (one word per device, shared by every
  * stream and call: a failure on any stream shows up in the next check).
- * Returns AAREN_OK, AAREN_ERR_LOOKBACK_TIMEOUT, AAREN_ERR_LOAD_TIMEOUT or
+ * Returns AAREN_OK, AAREN_ERR_BOUNDS (checked build), AAREN_ERR_LOAD_TIMEOUT,
+ * AAREN_ERR_LOOKBACK_TIMEOUT (in that order when several bits are set) or
  * AAREN_ERR_CUDA (a CUDA error from the synchronisation).
  */
 aaren_status_t aaren_check(void *stream);
@@ -299,20 +303,64 @@ int32_t aaren_abi_version(void);
 
 /*
  * aaren_debug_set_fault -- testing hook for the bounded waits.  Every later
- * scan launch in this process uses these values:
- *   never_publish_chunk  index (in launch order: head * ceil(N/C) + c) of a
- *        chunk whose carry is never published, so its successors must give
- *        up; -1 = none (the default).
- *   wait_limit_ns        how long a carry wait or a bulk-copy wait lasts
- *        before it gives up; <= 0 restores the default (1 s).
+ * launch of the scan, the scan with statistics and the backward pass in this
+ * process uses these values:
+ *   never_publish_chunk  index (head * chunks per head + c, c the chunk of
+ *        the head) of a chunk whose carry is never published, so the chunks
+ *        that wait on it give up: its successors in the forward scans
+ *        (chunks of aaren_scan_chunk_tokens tokens), its predecessors in the
+ *        backward pass (chunks of aaren_backward_chunk_tokens tokens);
+ *        -1 = none (the default).
+ *   wait_limit_ns        how long a device wait lasts before it gives up
+ *        (every kernel's waits; the persistent scan's waits inside a block
+ *        get 16 times as long); <= 0 restores the default (1 s).
  * Returns AAREN_OK.  Not for production use.
  */
 aaren_status_t aaren_debug_set_fault(int64_t never_publish_chunk,
                                      int64_t wait_limit_ns);
 
+/*
+ * aaren_debug_drop_arrival -- testing hook for the waits inside a block.
+ * Every later launch in this process withholds one arrival on a barrier
+ * between the warps of one block, so the warps waiting on it give up with
+ * AAREN_ERR_LOAD_TIMEOUT (reported by aaren_check) and the block leaves
+ * early, with no copy or tensor-core product still in flight:
+ *   - the persistent scan kernel (bfloat16 inputs, and float32 at d = 64):
+ *     the first compute warp of chunk `chunk` (numbered as for
+ *     aaren_debug_set_fault) does not report its partial aggregate;
+ *   - aaren_linattn_forward: in chunk `chunk` of the first thread block
+ *     (chunk c of head 0 for c < ceil(N/128)), the weighted keys are never
+ *     announced to the warp that issues the tensor-core products.
+ * -1 = none (the default).  Returns AAREN_OK.  Not for production use.
+ */
+aaren_status_t aaren_debug_drop_arrival(int64_t chunk);
+
+/*
+ * aaren_checked_build -- 1 in the checked build of this library
+ * (libaaren_checked.so, compiled with -DAAREN_CHECKED), 0 otherwise.  In the
+ * checked build every kernel tests each extent it computes (rows of a global
+ * tensor, a workspace slot, a bulk copy, a shared-memory stage) against its
+ * buffer before the access; a violation skips the access and makes
+ * aaren_check report AAREN_ERR_BOUNDS.  Results are otherwise identical.
+ */
+int32_t aaren_checked_build(void);
+
+/*
+ * aaren_debug_bounds_probe -- testing hook of the checked build: every later
+ * aaren_step adds `offset` to the stream index its bounds check tests (never
+ * to an address), so an offset >= n makes every stream's check fail, skip
+ * its accesses and report AAREN_ERR_BOUNDS.  No effect in the regular build.
+ * 0 = none (the default).  Returns AAREN_OK.  Not for production use.
+ */
+aaren_status_t aaren_debug_bounds_probe(int64_t offset);
+
 /* Tokens per chunk (one thread block) the scan uses for this d and dtype
  * (0 if unsupported); the chunk index of aaren_debug_set_fault counts these. */
 int64_t aaren_scan_chunk_tokens(int64_t d, int32_t dtype);
+
+/* Tokens per chunk of aaren_scan_backward for this d and dtype (0 if
+ * unsupported); aaren_debug_set_fault counts these in the backward pass. */
+int64_t aaren_backward_chunk_tokens(int64_t d, int32_t dtype);
 
 /*
  * aaren_scan_forward_noalloc -- aaren_scan_forward for callers that must not

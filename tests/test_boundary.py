@@ -37,10 +37,20 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings(lib):
-    for code in range(7):
+    for code in range(8):
         assert binding.status_string(code) and binding.status_string(code) != "unknown status"
     assert binding.status_string(99) == "unknown status"
-    assert binding.aaren_abi_version() == 1
+    assert binding.aaren_abi_version() == 2
+
+
+def test_binding_status_codes_match_the_header():
+    text = open(HEADER).read()
+    body = text[text.index("typedef enum {"):text.index("} aaren_status_t;")]
+    codes = dict(re.findall(r"(AAREN_\w+)\s*=\s*(\d+)", body))
+    assert codes, "no status codes found"
+    for name, value in codes.items():
+        assert getattr(binding, name) == int(value), name
+    assert codes["AAREN_ERR_BOUNDS"] == "5"
 
 
 def test_workspace_bytes(lib):
@@ -97,6 +107,8 @@ def test_argument_checks_before_any_cuda_call(lib):
 def test_debug_hook_is_host_state(lib):
     assert lib.aaren_debug_set_fault(5, 1000) == 0
     assert lib.aaren_debug_set_fault(-1, 0) == 0
+    assert lib.aaren_debug_drop_arrival(3) == 0
+    assert lib.aaren_debug_drop_arrival(-1) == 0
 
 
 def test_no_cpu_fallback_without_library(tmp_path):
