@@ -91,7 +91,7 @@ struct PipeTile {
     static constexpr size_t g_coef = g_cst + size_t(kPipeComputeWarps) * SS * sizeof(float);
     static constexpr size_t g_meta = g_coef + size_t(kPipeComputeWarps) * 32 * sizeof(float4);
     static constexpr size_t g_bars = g_meta + 16;
-    static constexpr size_t group_bytes = g_bars + 4 * sizeof(uint64_t);
+    static constexpr size_t group_bytes = g_bars + 6 * sizeof(uint64_t);   // 5 used, 16-byte multiple
     // Block: the stages, the groups, then the pool's free mask, the stages'
     // fill counters and their "full" mbarriers.
     static constexpr size_t group_off = size_t(STAGES) * stage_bytes;
@@ -257,7 +257,8 @@ __global__ void __launch_bounds__(PipeTile<D, GROUPS, STAGES, Tin>::THREADS, 1)
     uint64_t *metab = gbars + 0;    // the group's next chunk is known (carry warp)
     uint64_t *empty = gbars + 1;    // the chunk's stage has been read (4 compute warps)
     uint64_t *aggb = gbars + 2;     // warp aggregates written (4 compute warps)
-    uint64_t *carryb = gbars + 3;   // carries written (carry warp)
+    uint64_t *carryb = gbars + 3;   // the chunk's carry written (carry warp)
+    uint64_t *cagg = gbars + 4;     // the chunk aggregate written (compute warp 1)
     unsigned *pool = reinterpret_cast<unsigned *>(smem + T::pool_off);          // free stages
     unsigned *fills = reinterpret_cast<unsigned *>(smem + T::fills_off);        // per stage
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + T::full_off);          // per stage
@@ -275,6 +276,7 @@ __global__ void __launch_bounds__(PipeTile<D, GROUPS, STAGES, Tin>::THREADS, 1)
         ptx::mbar_init(empty, kPipeComputeWarps);
         ptx::mbar_init(aggb, kPipeComputeWarps);
         ptx::mbar_init(carryb, 1);
+        ptx::mbar_init(cagg, 1);
     }
     if (threadIdx.x == 0) ptx::fence_barrier_init();
     __syncthreads();
@@ -394,39 +396,23 @@ __global__ void __launch_bounds__(PipeTile<D, GROUPS, STAGES, Tin>::THREADS, 1)
             } else {
                 lb_ok = slot_ok && lookback<D, kPipeFoldBatch>(p, head, c, xm, xu, xw, lane);
             }
-            // chunk aggregate from the four warp aggregates
-            if (!wait_bar(aggb, par, group_limit)) {
+            // the chunk aggregate, formed by compute warp 1 (slot 1 of cst)
+            if (!wait_bar(cagg, par, group_limit)) {
                 if (lane == 0) atomicOr(p.status, STATUS_LOAD_TIMEOUT);
                 break;   // the compute warps stopped
             }
             held = -1;   // the compute warps have consumed the copy
-            float am, aw, au[E];
-            const float *wst_it = wst + par * WS;
-            chunk_aggregate<D>(wst_it, am, au, aw, lane);
             if (lb_ok) {
-                float im = am, iw = aw, iu[E];
-#pragma unroll
-                for (int e = 0; e < E; ++e) iu[e] = au[e];
-                combine_into<E>(xm, xu, xw, im, iu, iw);   // inclusive = exclusive (+) aggregate
-                // carry into compute warp k = exclusive (+) aggregates of warps
-                // 0..k-1, handed over before the inclusive prefix is published
-                // (only successors need that)
-#pragma unroll
-                for (int k = 0; k < kPipeComputeWarps; ++k) {
-                    write_state<D>(cst + k * SS, xm, xu, xw, lane);
-                    if (k + 1 < kPipeComputeWarps) {
-                        float bm, bw, bu[E];
-                        read_state_smem<D>(wst_it + k * SS, bm, bu, bw, lane);
-                        combine_into<E>(xm, xu, xw, bm, bu, bw);
-                        xm = bm;
-                        xw = bw;
-#pragma unroll
-                        for (int e = 0; e < E; ++e) xu[e] = bu[e];
-                    }
-                }
+                float im, iw, iu[E];
+                read_state_smem<D>(cst + SS, im, iu, iw, lane);
+                // the carry into the chunk (slot 0): each compute warp adds
+                // the aggregates of the warps before it itself, so the carry
+                // warp hands over one state and goes on to the inclusive prefix
+                write_state<D>(cst, xm, xu, xw, lane);
                 if (lane == 0) *fail = 0;
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(carryb);
+                combine_into<E>(xm, xu, xw, im, iu, iw);   // inclusive = exclusive (+) aggregate
                 if (publish) {
                     write_state<D>(my_state + SS, im, iu, iw, lane);
                     publish_flag(my_flag, FLAG_INC, lane);
@@ -569,34 +555,52 @@ __global__ void __launch_bounds__(PipeTile<D, GROUPS, STAGES, Tin>::THREADS, 1)
             __syncwarp();
         }
 
-        // 3. compute warp 1 publishes the chunk aggregate for successors'
-        //    look-backs as soon as the four warp aggregates exist (warp 0 is
-        //    busy handing the stage back; the wait for the carry would
-        //    otherwise be idle).  A successor's look-back waits for the
+        // 3. compute warp 1 forms the chunk aggregate as soon as the four
+        //    warp aggregates exist (warp 0 is busy handing the stage back;
+        //    the wait for the carry would otherwise be idle).  It hands it to
+        //    the carry warp (for the inclusive prefix) and publishes it for
+        //    successors' look-backs: a successor's look-back waits for the
         //    aggregates of every predecessor still in flight, so this
         //    publication sets the pace of the whole scan.  The carry warp
         //    may already have published the inclusive prefix, which wins.
-        if (wg == (kPipeComputeWarps > 1 ? 1 : 0) && c > 0) {
-            const int64_t chunk = head * p.chunks_per_head + c;
-            if (chunk != p.fault_chunk && rows_ok && compute_wait(aggb, par, group_limit)) {
+        if (wg == 1) {
+            if (compute_wait(aggb, par, group_limit)) {
                 float am, aw, au[E];
                 chunk_aggregate<D>(wst + par * WS, am, au, aw, lane);
-                write_state<D>(p.states + size_t(chunk) * 2 * SS, am, au, aw, lane);
-                publish_agg_if_none(p.flags + chunk, lane);
+                write_state<D>(cst + SS, am, au, aw, lane);
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(cagg);
+                const int64_t chunk = head * p.chunks_per_head + c;
+                if (c > 0 && chunk != p.fault_chunk && rows_ok) {
+                    write_state<D>(p.states + size_t(chunk) * 2 * SS, am, au, aw, lane);
+                    publish_agg_if_none(p.flags + chunk, lane);
+                }
             }
         }
 
-        // 4. wait for this warp's carry
+        // 4. wait for the chunk's carry
         if (!compute_wait(carryb, par, group_limit)) {
             if (lane == 0) atomicOr(p.status, STATUS_LOAD_TIMEOUT);
             break;
         }
         if (*fail) continue;
 
-        // 5. rescan from the carry, V from registers, and write O
+        // 5. this warp's carry = the chunk's carry (+) the aggregates of the
+        //    warps before it, in warp order; then rescan from it, V from
+        //    registers, and write O
         if (nv > 0 && rows_ok) {
             float rm, rw, u[E];
-            read_state_smem<D>(cst + wg * SS, rm, u, rw, lane);
+            read_state_smem<D>(cst, rm, u, rw, lane);
+#pragma unroll 1
+            for (int k = 0; k < wg; ++k) {
+                float bm, bw, bu[E];
+                read_state_smem<D>(wst + par * WS + k * SS, bm, bu, bw, lane);
+                combine_into<E>(rm, u, rw, bm, bu, bw);
+                rm = bm;
+                rw = bw;
+#pragma unroll
+                for (int e = 0; e < E; ++e) u[e] = bu[e];
+            }
             // scalar recurrences across lanes (lane = token)
             float M = s;
 #pragma unroll
