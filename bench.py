@@ -43,6 +43,7 @@ sys.path.insert(0, ROOT)
 FALLBACK_HBM_GBS = 6400.0
 CPU_SAMPLE_TOKENS = 1 << 18      # per head, cpu_baseline leg
 CPU_SAMPLE_MIN_S = 1.0           # cpu_baseline: repeat the sample until this much wall time
+CPU_SAMPLE_RUNS = 3              # cpu_baseline: timed runs averaged
 CPU_SAMPLE_MAX_PASSES = 100000   # passes are bounded by time (CPU_SAMPLE_MIN_S), not count
 METRIC = "Aaren scan tokens/s and achieved HBM GB/s (% of B300 peak), 1 GPU"
 
@@ -90,6 +91,19 @@ def whole_job_rate(units_per_rank, world, step_ms):
     `units_per_rank` in a step of `step_ms` (the slowest rank's): weak
     scaling, so the job's work grows with the number of ranks."""
     return world * units_per_rank / (step_ms * 1e-3)
+
+
+def e2e_pieces(wl):
+    """Head ranges [h0, h1) of the flattened B*H heads for the end-to-end
+    leg's copy/compute overlap: up to 8 pieces of at least 2 heads (a piece
+    of a single long head leaves the look-back too deep to keep up with the
+    copies); a workload under 256 MB of K and V is one piece."""
+    in_b = 2 if wl.dtype == "bf16" else 4
+    if wl.heads * wl.N * wl.d * 2 * in_b < (1 << 28) or wl.heads < 4:
+        return [(0, wl.heads)]
+    n = min(8, wl.heads // 2)
+    bounds = [round(i * wl.heads / n) for i in range(n + 1)]
+    return [(bounds[i], bounds[i + 1]) for i in range(n)]
 
 
 def workload(args):
@@ -263,10 +277,13 @@ class OracleTimer:
     """The float64 oracle, as it stands, timed on this host's cores.  `items`
     holds one head's inputs each; `fn(item, out)` runs the oracle on one head
     writing its output into `out`.  Inputs are drawn, every output array is
-    allocated and first-touched, and the thread pool is started (one untimed
-    pass) before any clock starts, so a timed pass is the oracle's own work.
-    run(min_s) repeats whole passes over the items until `min_s` seconds have
-    elapsed and returns (head-tokens/s, seconds, passes)."""
+    allocated and first-touched, and the thread pool is started before any
+    clock starts; warm(min_s) then runs untimed passes for `min_s` seconds
+    (drawing the inputs uses torch's CPU thread pool, whose idle workers keep
+    spinning on the cores for a while afterwards), so a timed pass is the
+    oracle's own work on quiet cores.  run(min_s) repeats whole passes over
+    the items until `min_s` seconds have elapsed and returns (head-tokens/s,
+    seconds, passes)."""
 
     def __init__(self, fn, items, tokens, d, threads):
         import numpy as np
@@ -274,7 +291,13 @@ class OracleTimer:
         self.fn, self.items, self.tokens, self.threads = fn, items, tokens, threads
         self.outs = [np.ones((tokens, d), dtype=np.float64) for _ in items]
         self.pool = ThreadPoolExecutor(max_workers=threads) if threads > 1 else None
-        self.one_pass()
+
+    def warm(self, min_s):
+        t0 = time.perf_counter()
+        while True:
+            self.one_pass()
+            if time.perf_counter() - t0 >= min_s:
+                break
 
     def _one(self, i):
         self.fn(self.items[i], self.outs[i])
@@ -320,14 +343,20 @@ def cpu_baseline_leg(wl, threads):
     first CPU_SAMPLE_TOKENS tokens of every head, and one thread over the
     first CPU_SAMPLE_TOKENS / 4 tokens of head 0."""
     t = scan_oracle_timer(wl, CPU_SAMPLE_TOKENS, threads)
-    rate, dt, passes = t.run(CPU_SAMPLE_MIN_S)
+    t.warm(CPU_SAMPLE_MIN_S)
+    runs = [t.run(CPU_SAMPLE_MIN_S) for _ in range(CPU_SAMPLE_RUNS)]   # as the reference arm's steps
+    rate = statistics.mean(r for r, _, _ in runs)
+    dt = sum(d for _, d, _ in runs)
+    passes = sum(n for _, _, n in runs)
     n, nh, used = t.tokens, len(t.items), t.threads
     t.close()
     cpu = {"value": rate, "unit": "head-tokens/s", "cores": used, "kind": "oracle",
-           "sample": f"the first {n} tokens of all {nh} heads ({n * nh} head-tokens), "
-                     f"{passes} passes, {dt:.1f} s wall on {used} threads "
-                     f"(about {dt * used:.0f} CPU-seconds)"}
+           "sample": f"the first {n} tokens of all {nh} heads ({n * nh} head-tokens): the mean of "
+                     f"{CPU_SAMPLE_RUNS} runs of at least {CPU_SAMPLE_MIN_S:.0f} s ({passes} passes, "
+                     f"{dt:.1f} s wall on {used} threads, about {dt * used:.0f} CPU-seconds), after "
+                     f"{CPU_SAMPLE_MIN_S:.0f} s of untimed passes"}
     t1 = scan_oracle_timer(wl, CPU_SAMPLE_TOKENS // 4, 1, heads=1)
+    t1.warm(0.2)
     r1, dt1, passes1 = t1.run(CPU_SAMPLE_MIN_S)
     t1.close()
     cpu["single_thread"] = {"value": r1, "unit": "head-tokens/s", "cores": 1,
@@ -355,6 +384,7 @@ def run_reference(args):
     out = args.out_dtype or wl.dtype
     threads = min(host_cores(), wl.heads)
     timer = scan_oracle_timer(wl, CPU_SAMPLE_TOKENS, threads)
+    timer.warm(CPU_SAMPLE_MIN_S)
     rates = []
     for i in range(args.warmup + args.steps):
         r, dt, passes = timer.run(CPU_SAMPLE_MIN_S if i >= args.warmup else 0.0)
@@ -506,13 +536,38 @@ def run_ours(args):
         hq.copy_(q); hK.copy_(K); hV.copy_(V)
         dq, dK, dV, dO = q, K, V, O          # device buffers are reused
         e2e_steps = max(1, min(args.steps, 3))
+        pieces = e2e_pieces(wl)
+        s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+        ev_in = [torch.cuda.Event() for _ in pieces]
+        ev_done = [torch.cuda.Event() for _ in pieces]
+        flat = lambda t: t.view(wl.heads, *t.shape[2:])
+        hKf, hVf, dKf, dVf = flat(hK), flat(hV), flat(dK), flat(dV)
+        hqf, dqf = hq.view(wl.heads, wl.d), dq.view(wl.heads, wl.d)
+        hOf, dOf = hO.view(wl.heads, *O.shape[2:]), dO.view(wl.heads, *O.shape[2:])
 
         def e2e_step():
-            dq.copy_(hq, non_blocking=True)
-            dK.copy_(hK, non_blocking=True)
-            dV.copy_(hV, non_blocking=True)
-            call(dq, dK, dV, dO)
-            hO.copy_(dO, non_blocking=True)
+            """Heads in pieces: the host->device copy of piece i+1 (copy
+            stream), the call on piece i (the compute stream) and the
+            device->host copy of piece i-1 (a second copy stream) overlap, so
+            the two transfer directions run at once."""
+            s_in.wait_stream(stream)
+            s_out.wait_stream(stream)
+            with torch.cuda.stream(s_in):
+                dq.copy_(hq, non_blocking=True)
+            for i, (h0, h1) in enumerate(pieces):
+                with torch.cuda.stream(s_in):
+                    dKf[h0:h1].copy_(hKf[h0:h1], non_blocking=True)
+                    dVf[h0:h1].copy_(hVf[h0:h1], non_blocking=True)
+                    ev_in[i].record(s_in)
+                stream.wait_event(ev_in[i])
+                n = h1 - h0
+                sub = lambda t: t[h0:h1].view(1, n, *t.shape[1:])
+                call(sub(dqf), sub(dKf), sub(dVf), sub(dOf))
+                ev_done[i].record(stream)
+                s_out.wait_event(ev_done[i])
+                with torch.cuda.stream(s_out):
+                    hOf[h0:h1].copy_(dOf[h0:h1], non_blocking=True)
+            stream.wait_stream(s_out)
 
         e2e_step()
         torch.cuda.synchronize()
@@ -535,7 +590,9 @@ def run_ours(args):
                "ms_per_step": e2e_ms, "steps": e2e_steps,
                "path": ("pinned host q,K,V -> device, aaren_scan_reduce, device o_N -> pinned host"
                         if reduce else
-                        "pinned host q,K,V -> device, aaren_scan_forward_ex, device O -> pinned host")}
+                        "pinned host q,K,V -> device, aaren_scan_forward_ex, device O -> pinned host"),
+               "pieces": f"{len(pieces)} piece(s) of heads; the host->device copy, the call and the "
+                         f"device->host copy of consecutive pieces overlap on three streams"}
         del hq, hK, hV, hO
 
     if rank != 0:
@@ -709,6 +766,7 @@ def run_linattn(args):
     cpu = None
     if rank == 0:
         t = la_oracle_timer(wl, LA_CPU_TOKENS, LA_CPU_HEADS, host_cores())
+        t.warm(CPU_SAMPLE_MIN_S)
         rate, dt, passes = t.run(CPU_SAMPLE_MIN_S)
         n, nh, used = t.tokens, len(t.items), t.threads
         t.close()
@@ -716,6 +774,7 @@ def run_linattn(args):
                "sample": f"the first {n} tokens of {nh} heads ({n * nh} head-tokens), {passes} passes, "
                          f"{dt:.1f} s wall on {used} threads"}
         t1 = la_oracle_timer(wl, LA_CPU_TOKENS, 1, 1)
+        t1.warm(0.2)
         r1, dt1, passes1 = t1.run(CPU_SAMPLE_MIN_S)
         t1.close()
         cpu["single_thread"] = {"value": r1, "unit": "head-tokens/s", "cores": 1,
@@ -771,11 +830,33 @@ def run_linattn(args):
     hO = torch.empty(O.shape, dtype=out_t, pin_memory=True)
     hQ.copy_(Q); hK.copy_(K); hV.copy_(V)
     e2e_steps = max(1, min(args.steps, 3))
+    pieces = e2e_pieces(wl)
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in pieces]
+    ev_done = [torch.cuda.Event() for _ in pieces]
+    flat = lambda t: t.view(wl.heads, *t.shape[2:])
+    hf = [flat(t) for t in (hQ, hK, hV)]
+    df = [flat(t) for t in (Q, K, V)]
+    hOf, dOf = flat(hO), flat(O)
 
     def e2e_step():
-        Q.copy_(hQ, non_blocking=True); K.copy_(hK, non_blocking=True); V.copy_(hV, non_blocking=True)
-        call(Q, K, V, O)
-        hO.copy_(O, non_blocking=True)
+        """Heads in pieces, the copies in and out of consecutive pieces
+        overlapping the calls (three streams), as for the scan."""
+        s_in.wait_stream(stream)
+        s_out.wait_stream(stream)
+        for i, (h0, h1) in enumerate(pieces):
+            with torch.cuda.stream(s_in):
+                for d_, h_ in zip(df, hf):
+                    d_[h0:h1].copy_(h_[h0:h1], non_blocking=True)
+                ev_in[i].record(s_in)
+            stream.wait_event(ev_in[i])
+            sub = lambda t: t[h0:h1].view(1, h1 - h0, *t.shape[1:])
+            call(*(sub(t) for t in df), sub(dOf))
+            ev_done[i].record(stream)
+            s_out.wait_event(ev_done[i])
+            with torch.cuda.stream(s_out):
+                hOf[h0:h1].copy_(dOf[h0:h1], non_blocking=True)
+        stream.wait_stream(s_out)
 
     e2e_step()
     torch.cuda.synchronize()
@@ -815,7 +896,9 @@ def run_linattn(args):
         "e2e": {"value": whole_job_rate(tokens, world, e2e_ms), "unit": "head-tokens/s",
                 "h2d_bytes_per_step": 3 * elems * 2, "d2h_bytes_per_step": elems * out_b,
                 "ms_per_step": e2e_ms, "steps": e2e_steps,
-                "path": "pinned host Q,K,V -> device, aaren_linattn_forward, device O -> pinned host"},
+                "path": "pinned host Q,K,V -> device, aaren_linattn_forward, device O -> pinned host",
+                "pieces": f"{len(pieces)} piece(s) of heads; the host->device copy, the call and the "
+                          f"device->host copy of consecutive pieces overlap on three streams"},
         "clocks": clocks.summary(),
     }
     print(json.dumps(line), flush=True)
@@ -833,6 +916,7 @@ def main():
         from attention_prefix_scan_02_b300 import inputs
         wl = inputs.WORKLOADS["linattn"]
         timer = la_oracle_timer(wl, LA_CPU_TOKENS, LA_CPU_HEADS, host_cores())
+        timer.warm(CPU_SAMPLE_MIN_S)
         rates = []
         for i in range(args.warmup + args.steps):
             r, dt, passes = timer.run(CPU_SAMPLE_MIN_S if i >= args.warmup else 0.0)
