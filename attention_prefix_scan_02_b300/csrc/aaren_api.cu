@@ -127,12 +127,14 @@ aaren_status_t launch_scan(const ScanParams &p, int64_t total_chunks, cudaStream
 // Shape of the persistent bfloat16 kernel per d: groups (five warps each,
 // one 128-token chunk in flight) and stages in the block's pool (K, V and q
 // of one chunk each; 64 KB at d = 128).  A group holds a stage only from its
-// copy until its chunk is scored, so fewer stages than groups suffice.
+// copy until its V rows are in registers, about a quarter of a chunk's
+// life, so fewer stages than groups suffice: at d = 128 two (measured as
+// fast as three), which leaves room for the groups' look-back fold buffers.
 #ifndef AAREN_PIPE_GROUPS_D128
 #define AAREN_PIPE_GROUPS_D128 4
 #endif
 #ifndef AAREN_PIPE_STAGES_D128
-#define AAREN_PIPE_STAGES_D128 3
+#define AAREN_PIPE_STAGES_D128 2
 #endif
 #ifndef AAREN_PIPE_GROUPS_D64
 #define AAREN_PIPE_GROUPS_D64 4

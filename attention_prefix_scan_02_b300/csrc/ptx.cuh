@@ -141,5 +141,23 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, unsigned by
         : "memory");
 }
 
+// 1-D bulk copy global -> shared without an L2 cache hint.
+__device__ __forceinline__ void bulk_g2s_plain(void *dst, const void *src, unsigned bytes, uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+
+// Order this thread's earlier generic-proxy accesses (and what they
+// synchronised with) before its later async-proxy (bulk copy) accesses of
+// global memory.
+__device__ __forceinline__ void fence_proxy_async_global()
+{
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 }  // namespace ptx
 }  // namespace aaren

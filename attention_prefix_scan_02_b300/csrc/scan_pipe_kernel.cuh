@@ -10,25 +10,31 @@
 // maximum).  What differs is how the work is laid out on an SM.
 //
 // One block per SM stays alive for the whole launch.  It holds GROUPS
-// independent groups; each group owns one shared-memory stage (K and V of a
-// 128-token chunk) and five warps:
-//   * four compute warps; warp w owns tokens [32w, 32w + 32) of the chunk
-//     and lane l owns dims [E l, E l + E) of every row:
-//       - scores: each lane forms its E-term share of q . k_t per row, then a
-//         transposed butterfly of shuffles leaves s_t on lane t;
-//       - V of the warp's rows is copied into registers (still bfloat16);
-//       - warp aggregate (m, u, w) from those registers into shared memory
-//         ("agg" mbarrier), and the stage is handed back ("empty" mbarrier);
-//       - after the carry arrives ("carry" mbarrier): rescan from registers
-//         and write O;
+// independent groups that share a small pool of shared-memory stages (K, V
+// and q of a 128-token chunk each); each group has five warps:
+//   * four compute warps; warp w owns tokens [32w, 32w + 32) of the chunk:
+//       - scores, lane = token: bfloat16 keys with the mixed-precision FMA,
+//         float32 keys with the compensated dot product (the functions the
+//         other kernels use, so every kernel sees the same scores);
+//       - V of the warp's rows is copied into registers (lane l owns dims
+//         [E l, E l + E)), the stage is handed back ("empty" mbarrier), and
+//         the warp aggregate (m, u, w) goes to shared memory ("agg");
+//       - compute warp 1 combines the four warp aggregates into the chunk
+//         aggregate, hands it to the carry warp ("cagg") and publishes it for
+//         successors' look-backs;
+//       - once the chunk's carry arrives ("carry"), each warp adds the
+//         aggregates of the warps before it, rescans from registers and
+//         writes O;
 //   * one carry warp that never holds V:
-//       - takes the group's chunk tickets (interleaved over heads: ticket =
-//         c * heads + head) and issues the 1-D bulk copies (TMA) of K and V;
+//       - claims a stage, takes the group's next chunk ticket (interleaved
+//         over heads: ticket = c * heads + head) and issues the 1-D bulk
+//         copies (TMA) of K, V and q;
 //       - runs the decoupled look-back over predecessor chunks while the
-//         compute warps are still scoring, publishing this chunk's aggregate
-//         as soon as the compute warps have produced it;
-//       - publishes the inclusive prefix, hands each compute warp its carry,
-//         and only then takes the group's next ticket.
+//         compute warps are still scoring; the predecessors' states come
+//         into a fold buffer of the group by bulk copies, one round trip to
+//         L2 per window;
+//       - hands the chunk's exclusive prefix to the compute warps, publishes
+//         the inclusive prefix, and only then takes the group's next ticket.
 // Taking a ticket only when the group is about to need it keeps chunks
 // flowing close to ticket order, so predecessors have usually published by
 // the time a chunk looks back; the load of the next chunk overlaps the
@@ -55,16 +61,17 @@ namespace aaren {
 
 constexpr int kPipeComputeWarps = 4;
 constexpr int kPipeGroupWarps = kPipeComputeWarps + 1;
-// predecessor states folded per memory round trip in the look-back
-#ifndef AAREN_PIPE_FOLD_BATCH
-#define AAREN_PIPE_FOLD_BATCH 6
-#endif
-constexpr int kPipeFoldBatch = AAREN_PIPE_FOLD_BATCH;
 // rows per unrolled block of the rescan loop (32: fully unrolled)
 #ifndef AAREN_PIPE_RESCAN_BLOCK
 #define AAREN_PIPE_RESCAN_BLOCK 4
 #endif
 constexpr int kRescanBlock = AAREN_PIPE_RESCAN_BLOCK;
+// predecessor states a look-back fold brings into shared memory at once
+#ifndef AAREN_PIPE_FOLD_SLOTS
+#define AAREN_PIPE_FOLD_SLOTS 24
+#endif
+constexpr int kFoldSlots = AAREN_PIPE_FOLD_SLOTS;
+static_assert(kFoldSlots >= 1 && kFoldSlots <= 32, "a fold round takes at most one window");
 static_assert(32 % kRescanBlock == 0, "rescan blocks must tile the warp's 32 rows");
 
 template <int D, int GROUPS_, int STAGES_, typename Tin_ = __nv_bfloat16>
@@ -98,10 +105,13 @@ struct PipeTile {
     static constexpr size_t pool_off = group_off + size_t(GROUPS) * group_bytes;
     static constexpr size_t fills_off = pool_off + 16;
     static constexpr size_t full_off = fills_off + (size_t(STAGES) * 4 + 7) / 8 * 8;
-    static constexpr size_t smem_bytes = full_off + size_t(STAGES) * sizeof(uint64_t);
+    // each group's look-back fold buffer: kFoldSlots predecessor states
+    static constexpr size_t fold_bytes = size_t(kFoldSlots) * SS * sizeof(float);
+    static constexpr size_t fold_off = (full_off + size_t(STAGES) * sizeof(uint64_t) + 15) / 16 * 16;
+    static constexpr size_t smem_bytes = fold_off + size_t(GROUPS) * fold_bytes;
     static_assert(half_bytes % 16 == 0 && stage_bytes % 16 == 0 && g_cst % 16 == 0 &&
                       g_coef % 16 == 0 && g_meta % 16 == 0 && group_bytes % 16 == 0 &&
-                      group_off % 16 == 0 && full_off % 8 == 0,
+                      group_off % 16 == 0 && full_off % 8 == 0 && fold_bytes % 16 == 0,
                   "shared-memory regions must stay aligned");
     static_assert(STAGES >= 1 && STAGES <= 32, "the pool's free mask is one word");
     static_assert(smem_bytes <= 227 * 1024, "stages do not fit in shared memory");
@@ -221,6 +231,119 @@ __device__ __forceinline__ void chunk_aggregate(const float *wst, float &am,
     }
 }
 
+// Decoupled look-back of chunk c (carry warp) whose fold reads the
+// predecessors' states through shared memory.  A window of 32 predecessors
+// is polled as in lookback(); once it resolves, the lanes of its first n
+// (up to kFoldSlots) predecessors each start one 1-D bulk copy of their
+// state into the group's fold buffer `fb`, all on the mbarrier `fbar`, so
+// the whole window's states cross from L2 in one round trip and occupy no
+// registers while in flight (folding them from registers took one round
+// trip per batch of six states).  The fold itself then reads shared
+// memory.  The states are published with release semantics and their flags
+// read with acquire; a proxy fence orders those acquires before the copies.
+// `fb_phase` is the parity of the fold barrier's next phase; `fb_busy` stays
+// true if a wait for copies gave up (the caller waits for them before the
+// block's shared memory can go).  False when a wait gave up or a
+// predecessor was poisoned.
+template <int D>
+__device__ bool lookback_bulk(const ScanParams &p, int64_t head, int64_t c, float &xm,
+                              float (&xu)[VLayout<D>::E], float &xw, int lane, float *fb, uint64_t *fbar,
+                              unsigned &fb_phase, bool &fb_busy, int64_t wait_limit)
+{
+    using L = VLayout<D>;
+    constexpr int E = L::E;
+    constexpr int SS = StateLayout<D>::SS;
+    const int64_t first = head * p.chunks_per_head;   // chunk 0 of this head
+    const bool owns = (L::LANES == 32 || lane < L::LANES);
+    // every predecessor slot read below lies in [first, first + c), inside the workspace
+    if (!AAREN_IN_BOUNDS(p.status, c <= p.chunks_per_head && in_range(first, c, p.heads * p.chunks_per_head)))
+        return false;
+    if (fb_busy) {   // copies of an earlier fold that gave up: let them land first
+        if (!wait_bar(fbar, fb_phase, wait_limit)) return false;
+        fb_busy = false;
+        fb_phase ^= 1u;
+    }
+    for (int64_t j0 = c - 1; j0 >= 0; j0 -= 32) {
+        const int64_t j = j0 - lane;
+        const bool has = (j >= 0);   // lanes before chunk 0 act as a stop
+        const unsigned *fp = p.flags + first + (has ? j : 0);
+        unsigned f = FLAG_INC;
+        unsigned inc = 0;
+        int k = 31;
+        uint64_t t0 = 0;
+        unsigned sleep_ns = 32;
+        for (unsigned polls = 0;; ++polls) {
+            if (has) f = ptx::ld_acquire(fp);
+            inc = __ballot_sync(kFull, f == FLAG_INC);
+            const unsigned none = __ballot_sync(kFull, f == FLAG_NONE);
+            const unsigned poison = __ballot_sync(kFull, f == FLAG_POISON);
+            k = inc ? __ffs(inc) - 1 : 31;
+            const unsigned upto = (k == 31) ? kFull : ((2u << k) - 1u);   // lanes 0..k
+            if (poison & upto) return false;
+            if (!(none & upto)) break;
+            if (polls == 0) t0 = ptx::globaltimer();
+            if (polls >= kMinWaitPolls) {
+                int give_up = 0;
+                if (lane == 0) give_up = int64_t(ptx::globaltimer() - t0) > p.wait_limit_ns;
+                if (__shfl_sync(kFull, give_up, 0)) return false;
+            }
+            __nanosleep(sleep_ns);
+            if (sleep_ns < 256) sleep_ns *= 2;
+        }
+        __syncwarp();   // every lane's acquire before any lane's copy
+        // predecessors 0..k of the window (lanes before chunk 0 are never
+        // copied: the first of them is the stop k, an identity)
+        const int last = (j0 - k >= 0) ? k : static_cast<int>(j0);   // the window's last real predecessor
+        for (int i0 = 0; i0 <= last; i0 += kFoldSlots) {
+            const int n = (last + 1 - i0 < kFoldSlots) ? last + 1 - i0 : kFoldSlots;
+            const int i = i0 + lane;
+            const unsigned fi = __shfl_sync(kFull, f, i & 31);   // as lane i saw it
+            if (lane == 0) ptx::mbar_arrive_expect_tx(fbar, static_cast<unsigned>(n) * SS * sizeof(float));
+            __syncwarp();
+            if (lane < n) {
+                const float *src = p.states + (size_t(first + (j0 - i)) * 2 + (fi == FLAG_INC ? 1 : 0)) * SS;
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // earlier reads of fb first
+                ptx::fence_proxy_async_global();
+                ptx::bulk_g2s_plain(fb + lane * SS, src, SS * sizeof(float), fbar);
+            }
+            fb_busy = true;
+            if (!wait_bar(fbar, fb_phase, wait_limit)) return false;
+            fb_busy = false;
+            fb_phase ^= 1u;
+            // fold x := (these states) (+) x: scalars lane-parallel, u per lane over its dims
+            float mi = -INFINITY, wi = 0.f;
+            if (lane < n) {
+                mi = fb[lane * SS];
+                wi = fb[lane * SS + 1];
+            }
+            const float M = fmaxf(warp_max(mi), xm);
+            const float ei = (lane < n) ? exp_rel(mi, M) : 0.f;
+            float acc[E];
+#pragma unroll
+            for (int e = 0; e < E; ++e) acc[e] = 0.f;
+#pragma unroll 4
+            for (int b = 0; b < n; ++b) {
+                const float eb = __shfl_sync(kFull, ei, b);
+                if (owns) {
+                    float v[E];
+                    load_vals<E>(fb + b * SS + 4 + lane * E, v);
+#pragma unroll
+                    for (int e = 0; e < E; ++e) acc[e] = fmaf(eb, v[e], acc[e]);
+                }
+            }
+            const float wsum = warp_sum(ei * wi);
+            const float ex = (xm == -INFINITY) ? 0.f : exp_rel(xm, M);
+#pragma unroll
+            for (int e = 0; e < E; ++e) xu[e] = fmaf(ex, xu[e], acc[e]);
+            xw = fmaf(ex, xw, wsum);
+            xm = M;
+            __syncwarp();   // every lane's reads of fb before the next copies
+        }
+        if (inc != 0) return true;   // lane k held an inclusive prefix (or the head start)
+    }
+    return true;
+}
+
 #ifndef AAREN_PIPE_SPIN_WAIT
 #define AAREN_PIPE_SPIN_WAIT 0
 #endif
@@ -259,6 +382,8 @@ __global__ void __launch_bounds__(PipeTile<D, GROUPS, STAGES, Tin>::THREADS, 1)
     uint64_t *aggb = gbars + 2;     // warp aggregates written (4 compute warps)
     uint64_t *carryb = gbars + 3;   // the chunk's carry written (carry warp)
     uint64_t *cagg = gbars + 4;     // the chunk aggregate written (compute warp 1)
+    uint64_t *fbar = gbars + 5;     // look-back states landed in the fold buffer (bulk copies)
+    float *fb = reinterpret_cast<float *>(smem + T::fold_off + size_t(g) * T::fold_bytes);
     unsigned *pool = reinterpret_cast<unsigned *>(smem + T::pool_off);          // free stages
     unsigned *fills = reinterpret_cast<unsigned *>(smem + T::fills_off);        // per stage
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + T::full_off);          // per stage
@@ -277,6 +402,7 @@ __global__ void __launch_bounds__(PipeTile<D, GROUPS, STAGES, Tin>::THREADS, 1)
         ptx::mbar_init(aggb, kPipeComputeWarps);
         ptx::mbar_init(carryb, 1);
         ptx::mbar_init(cagg, 1);
+        ptx::mbar_init(fbar, 1);
     }
     if (threadIdx.x == 0) ptx::fence_barrier_init();
     __syncthreads();
@@ -289,6 +415,8 @@ __global__ void __launch_bounds__(PipeTile<D, GROUPS, STAGES, Tin>::THREADS, 1)
         const uint64_t pol = ptx::policy_evict_first();
         int held = -1;                // stage with a copy this warp issued (its chunk not yet aggregated)
         unsigned held_par = 0;
+        unsigned fb_phase = 0;        // parity of the fold barrier's next phase
+        bool fb_busy = false;         // fold copies possibly still in flight
         // Claim a free stage of the block's pool, take the group's next
         // ticket and start the chunk's copies; or post a stop.  False when no
         // stage came free in time.
@@ -394,7 +522,8 @@ __global__ void __launch_bounds__(PipeTile<D, GROUPS, STAGES, Tin>::THREADS, 1)
                     if (owns) load_vals<E>(p.u_in + head * D + lane * E, xu);
                 }
             } else {
-                lb_ok = slot_ok && lookback<D, kPipeFoldBatch>(p, head, c, xm, xu, xw, lane);
+                lb_ok = slot_ok && lookback_bulk<D>(p, head, c, xm, xu, xw, lane, fb, fbar, fb_phase, fb_busy,
+                                                    group_limit);
             }
             // the chunk aggregate, formed by compute warp 1 (slot 1 of cst)
             if (!wait_bar(cagg, par, group_limit)) {
@@ -438,6 +567,7 @@ __global__ void __launch_bounds__(PipeTile<D, GROUPS, STAGES, Tin>::THREADS, 1)
         // A copy this warp issued can still be in flight only if the compute
         // warps stopped early: wait for it before the block's memory goes.
         if (held >= 0 && lane == 0) wait_bar(full + held, held_par, group_limit);
+        if (fb_busy && lane == 0) wait_bar(fbar, fb_phase, group_limit);   // fold copies still in flight
         return;
     }
 
