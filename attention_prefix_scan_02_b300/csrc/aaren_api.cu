@@ -136,6 +136,9 @@ aaren_status_t launch_scan(const ScanParams &p, int64_t total_chunks, cudaStream
 #ifndef AAREN_PIPE_STAGES_D128
 #define AAREN_PIPE_STAGES_D128 2
 #endif
+#ifndef AAREN_PIPE_STAGES_F32_D64
+#define AAREN_PIPE_STAGES_F32_D64 3
+#endif
 #ifndef AAREN_PIPE_GROUPS_D64
 #define AAREN_PIPE_GROUPS_D64 4
 #endif
@@ -147,7 +150,8 @@ struct PipeChoice {
     // float32 at d = 64 has the stage size of bfloat16 at d = 128 (64 KB)
     static constexpr int DE = (sizeof(Tin) == 4) ? 2 * D : D;
     static constexpr int GROUPS = (DE == 128) ? AAREN_PIPE_GROUPS_D128 : (DE == 64 ? AAREN_PIPE_GROUPS_D64 : 4);
-    static constexpr int STAGES = (DE == 128) ? AAREN_PIPE_STAGES_D128 : (DE == 64 ? AAREN_PIPE_STAGES_D64 : 4);
+    static constexpr int STAGES = (sizeof(Tin) == 4 && D == 64) ? AAREN_PIPE_STAGES_F32_D64
+                                  : (DE == 128) ? AAREN_PIPE_STAGES_D128 : (DE == 64 ? AAREN_PIPE_STAGES_D64 : 4);
 };
 
 int sm_count()

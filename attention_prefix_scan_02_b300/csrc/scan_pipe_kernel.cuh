@@ -66,12 +66,13 @@ constexpr int kPipeGroupWarps = kPipeComputeWarps + 1;
 #define AAREN_PIPE_RESCAN_BLOCK 4
 #endif
 constexpr int kRescanBlock = AAREN_PIPE_RESCAN_BLOCK;
-// predecessor states a look-back fold brings into shared memory at once
+// predecessor states a look-back fold brings into shared memory at once, at
+// most (fewer where the stages leave less room)
 #ifndef AAREN_PIPE_FOLD_SLOTS
 #define AAREN_PIPE_FOLD_SLOTS 24
 #endif
-constexpr int kFoldSlots = AAREN_PIPE_FOLD_SLOTS;
-static_assert(kFoldSlots >= 1 && kFoldSlots <= 32, "a fold round takes at most one window");
+constexpr int kFoldSlotsMax = AAREN_PIPE_FOLD_SLOTS;
+constexpr size_t kSmemPerBlock = 227 * 1024;   // opt-in shared memory of a block
 static_assert(32 % kRescanBlock == 0, "rescan blocks must tile the warp's 32 rows");
 
 template <int D, int GROUPS_, int STAGES_, typename Tin_ = __nv_bfloat16>
@@ -105,10 +106,15 @@ struct PipeTile {
     static constexpr size_t pool_off = group_off + size_t(GROUPS) * group_bytes;
     static constexpr size_t fills_off = pool_off + 16;
     static constexpr size_t full_off = fills_off + (size_t(STAGES) * 4 + 7) / 8 * 8;
-    // each group's look-back fold buffer: kFoldSlots predecessor states
-    static constexpr size_t fold_bytes = size_t(kFoldSlots) * SS * sizeof(float);
+    // each group's look-back fold buffer: FOLD predecessor states, as many
+    // as the room the stages leave allows, up to kFoldSlotsMax
     static constexpr size_t fold_off = (full_off + size_t(STAGES) * sizeof(uint64_t) + 15) / 16 * 16;
+    static constexpr size_t fold_room = kSmemPerBlock > fold_off ? kSmemPerBlock - fold_off : 0;
+    static constexpr int FOLD_FIT = int(fold_room / (size_t(GROUPS) * SS * sizeof(float)));
+    static constexpr int FOLD = FOLD_FIT < kFoldSlotsMax ? FOLD_FIT : kFoldSlotsMax;
+    static constexpr size_t fold_bytes = size_t(FOLD) * SS * sizeof(float);
     static constexpr size_t smem_bytes = fold_off + size_t(GROUPS) * fold_bytes;
+    static_assert(FOLD >= 4 && FOLD <= 32, "the look-back fold needs a few slots, and takes at most one window");
     static_assert(half_bytes % 16 == 0 && stage_bytes % 16 == 0 && g_cst % 16 == 0 &&
                       g_coef % 16 == 0 && g_meta % 16 == 0 && group_bytes % 16 == 0 &&
                       group_off % 16 == 0 && full_off % 8 == 0 && fold_bytes % 16 == 0,
@@ -234,7 +240,7 @@ __device__ __forceinline__ void chunk_aggregate(const float *wst, float &am,
 // Decoupled look-back of chunk c (carry warp) whose fold reads the
 // predecessors' states through shared memory.  A window of 32 predecessors
 // is polled as in lookback(); once it resolves, the lanes of its first n
-// (up to kFoldSlots) predecessors each start one 1-D bulk copy of their
+// (up to FOLD) predecessors each start one 1-D bulk copy of their
 // state into the group's fold buffer `fb`, all on the mbarrier `fbar`, so
 // the whole window's states cross from L2 in one round trip and occupy no
 // registers while in flight (folding them from registers took one round
@@ -245,7 +251,7 @@ __device__ __forceinline__ void chunk_aggregate(const float *wst, float &am,
 // true if a wait for copies gave up (the caller waits for them before the
 // block's shared memory can go).  False when a wait gave up or a
 // predecessor was poisoned.
-template <int D>
+template <int D, int FOLD>
 __device__ bool lookback_bulk(const ScanParams &p, int64_t head, int64_t c, float &xm,
                               float (&xu)[VLayout<D>::E], float &xw, int lane, float *fb, uint64_t *fbar,
                               unsigned &fb_phase, bool &fb_busy, int64_t wait_limit)
@@ -294,8 +300,8 @@ __device__ bool lookback_bulk(const ScanParams &p, int64_t head, int64_t c, floa
         // predecessors 0..k of the window (lanes before chunk 0 are never
         // copied: the first of them is the stop k, an identity)
         const int last = (j0 - k >= 0) ? k : static_cast<int>(j0);   // the window's last real predecessor
-        for (int i0 = 0; i0 <= last; i0 += kFoldSlots) {
-            const int n = (last + 1 - i0 < kFoldSlots) ? last + 1 - i0 : kFoldSlots;
+        for (int i0 = 0; i0 <= last; i0 += FOLD) {
+            const int n = (last + 1 - i0 < FOLD) ? last + 1 - i0 : FOLD;
             const int i = i0 + lane;
             const unsigned fi = __shfl_sync(kFull, f, i & 31);   // as lane i saw it
             if (lane == 0) ptx::mbar_arrive_expect_tx(fbar, static_cast<unsigned>(n) * SS * sizeof(float));
@@ -522,8 +528,8 @@ __global__ void __launch_bounds__(PipeTile<D, GROUPS, STAGES, Tin>::THREADS, 1)
                     if (owns) load_vals<E>(p.u_in + head * D + lane * E, xu);
                 }
             } else {
-                lb_ok = slot_ok && lookback_bulk<D>(p, head, c, xm, xu, xw, lane, fb, fbar, fb_phase, fb_busy,
-                                                    group_limit);
+                lb_ok = slot_ok && lookback_bulk<D, T::FOLD>(p, head, c, xm, xu, xw, lane, fb, fbar, fb_phase,
+                                                             fb_busy, group_limit);
             }
             // the chunk aggregate, formed by compute warp 1 (slot 1 of cst)
             if (!wait_bar(cagg, par, group_limit)) {

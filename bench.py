@@ -149,10 +149,11 @@ def describe(wl, out):
             else "no flush: K+V per step larger than the 126 MB L2"}
 
 
-# the source files each profiled kernel is built from (its own code and what it includes)
+# the source files each profiled kernel is built from (its own code, what it
+# includes, and the host file that picks its launch shape)
 KERNEL_SOURCES = {
-    "k_scan_pipe": ["scan_pipe_kernel.cuh", "scan_kernel.cuh", "common.cuh", "ptx.cuh"],
-    "k_linattn": ["linattn_kernel.cuh", "tc.cuh", "scan_kernel.cuh", "common.cuh", "ptx.cuh"],
+    "k_scan_pipe": ["scan_pipe_kernel.cuh", "scan_kernel.cuh", "common.cuh", "ptx.cuh", "aaren_api.cu"],
+    "k_linattn": ["linattn_kernel.cuh", "tc.cuh", "scan_kernel.cuh", "common.cuh", "ptx.cuh", "aaren_api.cu"],
 }
 
 
