@@ -33,20 +33,22 @@
 //         compute warps are still scoring; the predecessors' states come
 //         into a fold buffer of the group by bulk copies, one round trip to
 //         L2 per window;
-//       - hands the chunk's exclusive prefix to the compute warps, publishes
-//         the inclusive prefix, and only then takes the group's next ticket.
+//       - hands the chunk's exclusive prefix to the compute warps, takes the
+//         group's next ticket (claiming a stage and starting its copies), and
+//         then publishes this chunk's inclusive prefix.
 // Taking a ticket only when the group is about to need it keeps chunks
 // flowing close to ticket order, so predecessors have usually published by
 // the time a chunk looks back; the load of the next chunk overlaps the
 // rescan of the current one.  Keeping V out of the carry warp keeps the
 // register peak to the larger of the two roles.
 //
-// Forward progress: a ticket is taken only when its group's stage is free,
-// and its copy is issued at once; every group handles its chunks in ticket
-// order.  The smallest unfinished ticket is then always the one its group is
-// working on, and it waits only on smaller (finished) tickets.  Every wait is
-// bounded (%globaltimer); a wait that gives up sets a bit of the device
-// status word and the group stops.
+// Forward progress: a ticket is taken only with a stage in hand, and its
+// copy is issued at once; every group handles its chunks in ticket order, and
+// between taking a ticket and publishing the previous chunk's inclusive
+// prefix the carry warp waits on nothing.  The smallest unfinished ticket is
+// then always one its group is working on, and it waits only on smaller
+// (finished) tickets.  Every wait is bounded (%globaltimer); a wait that
+// gives up sets a bit of the device status word and the group stops.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -514,6 +516,7 @@ __global__ void __launch_bounds__(PipeTile<D, GROUPS, STAGES, Tin>::THREADS, 1)
             const bool slot_ok = AAREN_IN_BOUNDS(p.status, in_range(chunk, 1, p.heads * p.chunks_per_head) &&
                                                                in_range(head, 1, p.heads));
             const bool publish = (chunk != p.fault_chunk) && slot_ok;
+            bool issued = false;   // the group's next chunk was already started
             unsigned *my_flag = p.flags + chunk;
             float *my_state = p.states + size_t(chunk) * 2 * SS;
 
@@ -547,6 +550,11 @@ __global__ void __launch_bounds__(PipeTile<D, GROUPS, STAGES, Tin>::THREADS, 1)
                 if (lane == 0) *fail = 0;
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(carryb);
+                // the group's next chunk starts now: what is left of this one
+                // (its inclusive prefix) waits on nothing, so its successors
+                // are not held up and tickets still finish in order
+                live = issue();
+                issued = true;
                 combine_into<E>(xm, xu, xw, im, iu, iw);   // inclusive = exclusive (+) aggregate
                 if (publish) {
                     write_state<D>(my_state + SS, im, iu, iw, lane);
@@ -568,7 +576,7 @@ __global__ void __launch_bounds__(PipeTile<D, GROUPS, STAGES, Tin>::THREADS, 1)
                 if (lane == 0) ptx::mbar_arrive(carryb);
                 if (publish) publish_flag(my_flag, FLAG_POISON, lane);
             }
-            live = issue();
+            if (!issued) live = issue();
         }
         // A copy this warp issued can still be in flight only if the compute
         // warps stopped early: wait for it before the block's memory goes.

@@ -56,6 +56,7 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="long", choices=["tiny", "bf16_4k", "stress", "long"])
     ap.add_argument("--heads", type=int, default=0, help="override H (profiling small cases)")
+    ap.add_argument("--batch", type=int, default=0, help="override B (profiling small cases)")
     ap.add_argument("--tokens", type=int, default=0, help="override N (profiling small cases)")
     ap.add_argument("--out-dtype", default="", choices=["", "bf16", "f32"])
     ap.add_argument("--op", default="scan", choices=["scan", "reduce", "backward", "step", "linattn"],
@@ -109,8 +110,8 @@ def e2e_pieces(wl):
 def workload(args):
     from attention_prefix_scan_02_b300 import inputs
     wl = inputs.WORKLOADS[args.workload]
-    if args.heads or args.tokens:
-        wl = inputs.custom(wl.B, args.heads or wl.H, args.tokens or wl.N, wl.d, wl.dtype, wl.seed,
+    if args.heads or args.tokens or args.batch:
+        wl = inputs.custom(args.batch or wl.B, args.heads or wl.H, args.tokens or wl.N, wl.d, wl.dtype, wl.seed,
                            wl.kind, wl.name if not args.tokens else f"{wl.name}_N{args.tokens}")
     return wl
 
@@ -761,6 +762,8 @@ def run_linattn(args):
     from attention_prefix_scan_02_b300 import binding, build, inputs
     build.build()
     wl = inputs.WORKLOADS["linattn"]
+    if args.batch:   # a smaller case for profiling: fewer sequences of the same recipe
+        wl = inputs.custom(args.batch, wl.H, wl.N, wl.d, wl.dtype, wl.seed, wl.kind, f"{wl.name}_B{args.batch}")
     out = args.out_dtype or wl.dtype
     out_t = torch.bfloat16 if out == "bf16" else torch.float32
     warmup = max(3, args.warmup)
@@ -886,7 +889,8 @@ def run_linattn(args):
                                f"Q, K, V ~ N(0,1) (a query per token), M = N, seed {wl.seed}",
                    "op": "linattn", "global_batch": world * wl.B,
                    "parallelism": f"independent sequences, {world} rank(s), no collective",
-                   "l2": "no flush: Q, K, V per step (1.07 GB) far larger than the 126 MB L2"},
+                   "l2": f"no flush: Q, K, V per step ({3 * wl.heads * wl.N * wl.d * 2 / 1e9:.2f} GB) larger than "
+                         f"the 126 MB L2"},
         "gpu_launches": args.steps,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak,
