@@ -32,9 +32,10 @@
 // One persistent CTA per SM walks whole heads (h = blockIdx.x, += gridDim.x)
 // chunk by chunk (g counts this CTA's chunks).  Roles:
 //   warp 0, one thread   tiled TMA loads of Q, K, V (two stages)
-//   warp 1, one thread   issues the MMAs as their operands become ready: MMA1,
-//       then MMA4, MMA3 and MMA2 in whatever order their inputs arrive (one
-//       commit for MMA4, one for MMA3 + MMA2)
+//   warp 1, one thread   issues MMA1, then MMA3 and MMA2 in whatever order
+//       their inputs arrive (one commit for both)
+//   warp 2, one thread   issues MMA4 once the weighted keys are written (a
+//       second issuing thread: one thread issues about one MMA per 33 ns)
 //   two row warpgroups (warps 4-7 and 8-11, thread = token row i = TMEM
 //       lane; warpgroup hf takes columns 64hf.. of P and dims 32hf.. of O):
 //       ReLU of Q and K in place (half of each row each); P -> A (causal
@@ -106,7 +107,8 @@ struct Bars {
     uint64_t aready;              // A in tensor memory (both row warpgroups): MMA2
     uint64_t pfull, dsfull, ofull;   // MMA completion (commit)
     uint64_t tfree;               // inter / intra read (both row warpgroups)
-    uint64_t drain;               // after a give-up: every MMA issued so far has completed
+    uint64_t drain, drain4;       // after a give-up: every MMA issued so far (by the MMA warp,
+                                  // by the MMA4 warp) has completed
     uint32_t tmem;
     int abort;
 };
@@ -248,7 +250,7 @@ k_linattn(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtens
         ptx::mbar_init(&b.kw, 1); ptx::mbar_init(&b.sready, 1); ptx::mbar_init(&b.aready, 2);
         ptx::mbar_init(&b.pfull, 1); ptx::mbar_init(&b.dsfull, 1); ptx::mbar_init(&b.ofull, 1);
         ptx::mbar_init(&b.tfree, 2);
-        ptx::mbar_init(&b.drain, 1);
+        ptx::mbar_init(&b.drain, 1); ptx::mbar_init(&b.drain4, 1);
         b.abort = 0;
         ptx::fence_barrier_init();
     }
@@ -297,66 +299,89 @@ k_linattn(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtens
             for (int64_t k = g - 2 > 0 ? g - 2 : 0; k < g; ++k)
                 wait_bar(&b.full[k & 1], static_cast<unsigned>((k >> 1) & 1), p.wait_limit_ns);
         }
-    } else if (warp == 1) {
-        // ---------------- MMA issue ----------------
-        if (lane == 0) {
-            const uint32_t kw0 = tc::saddr(sm + OFF_KW), s0 = tc::saddr(sm + OFF_S);
-            const uint32_t ones = tc::saddr(sm + OFF_ONES);
+    } else if (warp == 1 || warp == 2) {
+        // ---------------- MMA issue: warp 1 MMA1, MMA3, MMA2; warp 2 MMA4 ----------------
+        // Two issuing threads: one thread issues an MMA about every 33 ns
+        // whatever its size, and MMA4 (the state update) and MMA2 (intra) are
+        // both narrow (N = 80), so together they keep the tensor pipe busier.
+        // Descriptors of each operand's first K step are built once.  A step
+        // of `off` bytes adds off >> 4 to the descriptor's start-address
+        // field, which never carries out of it: every shared address here is
+        // below 256 KB, so (address >> 4) stays below 2^14.  The products are
+        // fully unrolled, so issuing one MMA costs an add and the instruction.
+        const uint32_t ones = tc::saddr(sm + OFF_ONES);
+        uint64_t dq[2], dk[2], dv[2];
+#pragma unroll
+        for (int s = 0; s < 2; ++s) {
+            const uint32_t q0 = tc::saddr(sm + OFF_STAGE + s * 3 * kTile);
+            dq[s] = tc::sdesc(q0, 16, 1024);
+            dk[s] = tc::sdesc(q0 + kTile, 16, 1024);
+            dv[s] = tc::sdesc(q0 + 2 * kTile, ones - (q0 + 2 * kTile), 1024);
+        }
+        if (warp == 2 && lane == 0) {
+            // MMA4: dS of chunk g once its weighted keys are written (which
+            // the key warpgroup does only after reading the previous dS)
+            const uint64_t dkw = tc::sdesc(tc::saddr(sm + OFF_KW), kTile, 1024);
+            bool issued = false;
+            for (int64_t g = 0; g < total; ++g) {
+                if (!la_wait(b, &b.kw, static_cast<unsigned>(g & 1), p)) break;
+                const uint64_t bv = (g & 1) ? dv[1] : dv[0];
+                tc::fence_after();
+#pragma unroll
+                for (int hl = 0; hl < 2; ++hl)
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)
+                        tc::mma_ss(tmem + COL_DS, dkw + ((hl * 2 * kTile + kk * 2048) >> 4), bv + 128 * kk, ID_KV,
+                                   hl > 0 || kk > 0);
+                tc::commit(&b.dsfull);
+                issued = true;
+            }
+            // gave up: let this thread's MMAs finish before tensor memory is freed
+            if (aborted(b) && issued) {
+                tc::commit(&b.drain4);
+                wait_bar(&b.drain4, 0, p.wait_limit_ns);
+            }
+        } else if (warp == 1 && lane == 0) {
+            const uint64_t dsz = tc::sdesc(tc::saddr(sm + OFF_S), 8192, 1024);
             const uint64_t *last = nullptr;   // the latest commit (null: no MMA issued yet)
             for (int64_t g = 0; g < total; ++g) {
                 const int s = static_cast<int>(g & 1);
                 const unsigned par = static_cast<unsigned>(g & 1), prev = par ^ 1u;
-                const uint32_t q0 = tc::saddr(sm + OFF_STAGE + s * 3 * kTile);
-                const uint32_t k0 = q0 + kTile, v0 = q0 + 2 * kTile;
+                const uint64_t aq = s ? dq[1] : dq[0], ak = s ? dk[1] : dk[0], bv = s ? dv[1] : dv[0];
                 la_wait(b, &b.qk[s], static_cast<unsigned>((g >> 1) & 1), p);
                 if (g > 0) la_wait(b, &b.ofull, prev, p);   // MMA2 of the previous chunk has read A
                 if (aborted(b)) break;
                 tc::fence_after();
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    tc::mma_ss(tmem + COL_P, tc::sdesc(q0 + kk * 32, 16, 1024), tc::sdesc(k0 + kk * 32, 16, 1024),
-                               ID_QK, kk > 0);
+                    tc::mma_ss(tmem + COL_P, aq + 2 * kk, ak + 2 * kk, ID_QK, kk > 0);
                 tc::commit(&b.pfull);
                 last = &b.pfull;
-                // MMA4 (state update), MMA3 (inter) and MMA2 (intra) as their
-                // operands come ready, in whatever order that is; the output
-                // barrier covers MMA3 and MMA2, MMA4 has its own
-                bool d4 = false, d3 = false, d2 = false, dO = false, tf = (g == 0), timed_out = false;
+                // MMA3 (inter) and MMA2 (intra) as their operands come ready,
+                // in whatever order that is; one output commit covers both
+                bool d3 = false, d2 = false, dO = false, tf = (g == 0), timed_out = false;
                 const uint64_t t_start = ptx::globaltimer();
-                for (unsigned polls = 0; !(d4 && dO); ++polls) {
+                for (unsigned polls = 0; !dO; ++polls) {
                     bool any = false;
-                    if (!d4 && ptx::mbar_test_wait(&b.kw, par)) {
-                        tc::fence_after();
-#pragma unroll 1
-                        for (int hl = 0; hl < 2; ++hl)
-#pragma unroll
-                            for (int kk = 0; kk < 8; ++kk)
-                                tc::mma_ss(tmem + COL_DS, tc::sdesc(kw0 + hl * 2 * kTile + kk * 2048, kTile, 1024),
-                                           tc::sdesc(v0 + kk * 2048, ones - v0, 1024), ID_KV, hl > 0 || kk > 0);
-                        tc::commit(&b.dsfull);
-                        last = &b.dsfull;
-                        d4 = any = true;
-                    }
                     if (!tf) tf = ptx::mbar_test_wait(&b.tfree, prev);   // inter / intra of the previous chunk read
                     if (tf && !d3 && ptx::mbar_test_wait(&b.sready, par)) {
                         tc::fence_after();
-#pragma unroll 1
+#pragma unroll
                         for (int hl = 0; hl < 2; ++hl)
 #pragma unroll
                             for (int kk = 0; kk < 4; ++kk)
-                                tc::mma_ss(tmem + COL_I, tc::sdesc(q0 + kk * 32, 16, 1024),
-                                           tc::sdesc(s0 + hl * kSPart + kk * 2048, 8192, 1024), ID_QS,
+                                tc::mma_ss(tmem + COL_I, aq + 2 * kk, dsz + ((hl * kSPart + kk * 2048) >> 4), ID_QS,
                                            hl > 0 || kk > 0);
                         d3 = any = true;
                     }
                     if (tf && !d2 && ptx::mbar_test_wait(&b.aready, par)) {
                         tc::fence_after();
-#pragma unroll 1
+#pragma unroll
                         for (int hl = 0; hl < 2; ++hl)
 #pragma unroll
                             for (int kk = 0; kk < 8; ++kk)
                                 tc::mma_ts(tmem + COL_X, tmem + COL_P + 32 * (kk >> 1) + 16 * hl + 8 * (kk & 1),
-                                           tc::sdesc(v0 + kk * 2048, ones - v0, 1024), ID_AV, hl > 0 || kk > 0);
+                                           bv + 128 * kk, ID_AV, hl > 0 || kk > 0);
                         d2 = any = true;
                     }
                     if (d2 && d3 && !dO) {   // exactly one output commit per chunk
@@ -534,19 +559,21 @@ k_linattn(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtens
             load_start(blockIdx.x);
             publish_state();   // the first chunk's state
         }
+        // head and chunk of chunk g, and the angle of this thread's token row
+        // in it (the next chunk's is computed while MMA4 runs)
+        int64_t h = blockIdx.x, c = 0;
+        float cs, sn;
+        pos_angle(p.pos0 + r + 1, p.inv_2M, cs, sn);
         for (int64_t g = 0; g < total; ++g) {
             if (stop_all(3, aborted(b))) break;
             const int s = static_cast<int>(g & 1);
             const unsigned par = static_cast<unsigned>(g & 1);
-            const int64_t h = blockIdx.x + (g / nc) * gridDim.x, c = g % nc;
 
             // ---- keys (ReLU'd by the row warpgroups): cos / sin weighted as hi/lo (MMA4);
             //      the previous chunk's MMA4 is done with the buffer (dsfull waited below) ----
             la_wait(b, &b.qk[s], static_cast<unsigned>((g >> 1) & 1), p);
             {
                 const uint8_t *krow = sm + OFF_STAGE + s * 3 * kTile + kTile + r * 128;
-                float cs, sn;
-                pos_angle(p.pos0 + c * C + r + 1, p.inv_2M, cs, sn);
                 const uint64_t c2 = f2(cs, cs), s2 = f2(sn, sn);
 #pragma unroll
                 for (int ch = 0; ch < 8; ++ch) {
@@ -571,25 +598,31 @@ k_linattn(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtens
             tc::fence_before();
             ptx::named_bar_sync(3, 128);
             if (r == 0 && !(blockIdx.x == 0 && g == p.drop_chunk)) ptx::mbar_arrive(&b.kw);
+            const bool head_end = c == nc - 1;
+            {
+                const int64_t pos1 = head_end ? 0 : (c + 1) * C;
+                pos_angle(p.pos0 + pos1 + r + 1, p.inv_2M, cs, sn);   // the next chunk's angle
+            }
 
             // ---- dS, dz of this chunk; then the stage is no longer read here or by MMA4 ----
             la_wait(b, &b.dsfull, par, p);
             tc::fence_after();
             __syncwarp();
-#pragma unroll
-            for (int b0 = 0; b0 < 64; b0 += 32) {
-                float dv[32];
-                tc::ld32(tmem + lane_base + COL_DS + b0, dv);
-#pragma unroll
-                for (int t = 0; t < 32; ++t) S[b0 + t] += dv[t];
-            }
             {
-                float dz, dz1;
-                tc::ld2(tmem + lane_base + COL_DS + 64, dz, dz1);
-                z += dz;
+                uint32_t dv[32], dz, dz1;
+                tc::ld32_async(tmem + lane_base + COL_DS, dv);
+                tc::ld2_async(tmem + lane_base + COL_DS + 64, dz, dz1);
+                tc::wait_ld();
+#pragma unroll
+                for (int t = 0; t < 32; ++t) S[t] += __uint_as_float(dv[t]);
+                z += __uint_as_float(dz);
+                tc::ld32_async(tmem + lane_base + COL_DS + 32, dv);
+                tc::wait_ld();
+#pragma unroll
+                for (int t = 0; t < 32; ++t) S[32 + t] += __uint_as_float(dv[t]);
             }
             if (r == 0) ptx::mbar_arrive(&b.empty[s]);
-            if (c == nc - 1) {   // end of a head: its final state, then the next head's start
+            if (head_end) {   // end of a head: its final state, then the next head's start
                 if (p.S_out != nullptr && !aborted(b) && AAREN_IN_BOUNDS(p.status, in_range(h, 1, p.BH))) {
                     float4 *dst = reinterpret_cast<float4 *>(p.S_out + ((h * 2 + half) * 64 + k) * 64);
 #pragma unroll
@@ -604,6 +637,12 @@ k_linattn(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtens
             if (g + 1 < total) {
                 la_wait(b, &b.ofull, par, p);
                 publish_state();
+            }
+            if (head_end) {
+                c = 0;
+                h += gridDim.x;
+            } else {
+                ++c;
             }
         }
     }
