@@ -523,6 +523,7 @@ aaren_status_t aaren_linattn_forward(const void *Q, const void *K, const void *V
     p.S_in = S_in; p.z_in = z_in; p.S_out = S_out; p.z_out = z_out;
     p.BH = BH; p.N = N; p.pos0 = pos0;
     p.inv_2M = 1.0 / (2.0 * M);
+    p.inv_2Mf = static_cast<float>(p.inv_2M);
     p.status = status;
     p.wait_limit_ns = g_wait_limit_ns.load();
     p.drop_chunk = g_drop_chunk.load();

@@ -93,6 +93,7 @@ struct Params {
     float *S_out, *z_out;       // same layout or null
     int64_t BH, N, pos0;
     double inv_2M;              // position * inv_2M = angle / pi
+    float inv_2Mf;              // the same in single precision
     unsigned *status;
     int64_t wait_limit_ns;
     int64_t drop_chunk;         // testing: chunk (of CTA 0) whose weighted keys are never
@@ -208,10 +209,17 @@ __device__ __forceinline__ void store_row32(__nv_bfloat16 *dst, const float (&o)
                        bf2_bits(o[t + 6], o[t + 7]));
 }
 
-// (cos, sin) of the angle of 1-based position pos: pi/2 * pos / M.
-__device__ __forceinline__ void pos_angle(int64_t pos, double inv_2M, float &cs, float &sn)
+// (cos, sin) of the angle of 1-based position pos: pi/2 * pos / M, with
+// inv_2Mf = 1 / (2M) in single precision.  The argument carries at most three
+// units in the last place of relative error (the conversion of pos, exact
+// below 2^24, inv_2Mf and the product) against one when the product is taken
+// in double precision and rounded; either way it is then a float.  The empty
+// asm keeps the computation where it is called, off the path that first
+// reads the values.
+__device__ __forceinline__ void pos_angle(int64_t pos, float inv_2Mf, float &cs, float &sn)
 {
-    sincospif(static_cast<float>(static_cast<double>(pos) * inv_2M), &sn, &cs);
+    sincospif(static_cast<float>(pos) * inv_2Mf, &sn, &cs);
+    asm volatile("" : "+f"(cs), "+f"(sn));
 }
 
 // ReLU of half of one 128-byte row (row index r, half hf: slots visited 4hf
@@ -324,8 +332,8 @@ k_linattn(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtens
             const uint64_t dkw = tc::sdesc(tc::saddr(sm + OFF_KW), kTile, 1024);
             bool issued = false;
             for (int64_t g = 0; g < total; ++g) {
-                if (!la_wait(b, &b.kw, static_cast<unsigned>(g & 1), p)) break;
                 const uint64_t bv = (g & 1) ? dv[1] : dv[0];
+                if (!la_wait(b, &b.kw, static_cast<unsigned>(g & 1), p)) break;
                 tc::fence_after();
 #pragma unroll
                 for (int hl = 0; hl < 2; ++hl)
@@ -428,13 +436,13 @@ k_linattn(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtens
             ptx::named_bar_sync(nb, 128);
             if (leader) ptx::mbar_arrive(&b.qk[0]);
         }
+        int64_t h = blockIdx.x, c = 0;   // head and chunk of chunk g
         for (int64_t g = 0; g < total; ++g) {
             if (stop_all(nb, aborted(b))) break;
             const int s = static_cast<int>(g & 1);
             const unsigned par = static_cast<unsigned>(g & 1);
-            const int64_t h = blockIdx.x + (g / nc) * gridDim.x, c = g % nc;
             float cs, sn;
-            pos_angle(p.pos0 + c * C + i + 1, p.inv_2M, cs, sn);
+            pos_angle(p.pos0 + c * C + i + 1, p.inv_2Mf, cs, sn);
 
             // ---- P -> A on columns 64 hf .. 64 hf + 63: causal mask and cos weight, hi/lo ----
             la_wait(b, &b.pfull, par, p);
@@ -492,7 +500,7 @@ k_linattn(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtens
                 tc::ld2_async(tmem + lane_base + COL_I + 128, z0, z1);
                 tc::wait_ld();
                 const float dt = __uint_as_float(d0) + cs * __uint_as_float(z0) + sn * __uint_as_float(z1);
-                const float r = dt != 0.f ? 1.f / dt : 0.f;
+                const float r = dt != 0.f ? __frcp_rn(dt) : 0.f;   // correctly rounded, as 1 / dt
                 float o[32];
 #pragma unroll
                 for (int t = 0; t < 32; ++t)
@@ -506,6 +514,10 @@ k_linattn(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtens
             if (leader) {
                 ptx::mbar_arrive(&b.tfree);
                 ptx::mbar_arrive(&b.empty[s]);
+            }
+            if (++c == nc) {
+                c = 0;
+                h += gridDim.x;
             }
         }
     } else if (warp >= 12) {
@@ -563,7 +575,7 @@ k_linattn(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtens
         // in it (the next chunk's is computed while MMA4 runs)
         int64_t h = blockIdx.x, c = 0;
         float cs, sn;
-        pos_angle(p.pos0 + r + 1, p.inv_2M, cs, sn);
+        pos_angle(p.pos0 + r + 1, p.inv_2Mf, cs, sn);
         for (int64_t g = 0; g < total; ++g) {
             if (stop_all(3, aborted(b))) break;
             const int s = static_cast<int>(g & 1);
@@ -601,7 +613,7 @@ k_linattn(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtens
             const bool head_end = c == nc - 1;
             {
                 const int64_t pos1 = head_end ? 0 : (c + 1) * C;
-                pos_angle(p.pos0 + pos1 + r + 1, p.inv_2M, cs, sn);   // the next chunk's angle
+                pos_angle(p.pos0 + pos1 + r + 1, p.inv_2Mf, cs, sn);   // the next chunk's angle
             }
 
             // ---- dS, dz of this chunk; then the stage is no longer read here or by MMA4 ----

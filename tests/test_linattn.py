@@ -152,6 +152,23 @@ def test_continuation_from_a_state():
     assert eS <= TOL_LA and ez <= TOL_LA
 
 
+@pytest.mark.parametrize("out", ["f32", "bf16"])
+def test_positions_past_single_precision(out):
+    """Positions that continue from near 2^24, where their conversion to
+    single precision stops being exact (the kernel forms each angle as
+    float(position) / (2M) in single precision)."""
+    out_t = torch.float32 if out == "f32" else torch.bfloat16
+    Q, K, V = workload(1, 2, 300, 77)
+    pos0 = (1 << 24) - 150
+    M = float(pos0 + 300)
+    O, (S, z) = run(Q, K, V, out_t, M=M, pos0=pos0)
+    Or, Sr, zr = ref_heads(Q, K, V, M, pos0=pos0)
+    check_out(f"la_far_positions_{out}", O, Or, out_t)
+    eS, ez = state_err(S, z, Sr, zr)
+    report(f"la_far_positions_{out}_state", S=eS, z=ez)
+    assert eS <= TOL_LA and ez <= TOL_LA
+
+
 def test_zero_queries_give_zero_rows():
     Q, K, V = workload(1, 2, 400, 75)
     rows = [0, 5, 127, 128, 333]
