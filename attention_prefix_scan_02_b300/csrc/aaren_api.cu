@@ -220,9 +220,20 @@ template <int D, typename Tin, typename Tout>
 aaren_status_t launch_step(const StepParams &p, cudaStream_t st)
 {
     const int64_t threads = p.n * 32;
-    const unsigned blocks = unsigned((threads + 255) / 256);
-    k_step<D, Tin, Tout><<<blocks, 256, 0, st>>>(p);
-    return cudaGetLastError() == cudaSuccess ? AAREN_OK : AAREN_ERR_CUDA;
+    // programmatic stream serialisation: the step may begin launching while
+    // the kernel before it finishes; k_step waits for that kernel's completion
+    // (griddepcontrol.wait) before it reads anything
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned((threads + 255) / 256));
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k_step<D, Tin, Tout>, p) == cudaSuccess ? AAREN_OK : AAREN_ERR_CUDA;
 }
 
 template <int D>

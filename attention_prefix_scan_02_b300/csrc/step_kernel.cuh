@@ -33,6 +33,12 @@ __global__ void __launch_bounds__(256) k_step(const StepParams p)
 {
     using L = VLayout<D>;
     constexpr int E = L::E;
+    // Launched as a programmatic dependent of the kernel before it in the
+    // stream (usually the previous step): wait until that kernel has completed
+    // and its writes are visible, then let the next step's launch begin, so
+    // that launch overlaps this step's work.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int lane = threadIdx.x & 31;
     const int64_t i = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     if (i >= p.n) return;   // uniform per warp
