@@ -35,7 +35,8 @@
 //   warp 1, one thread   issues MMA1, then MMA3 and MMA2 in whatever order
 //       their inputs arrive (one commit for both)
 //   warp 2, one thread   issues MMA4 once the weighted keys are written (a
-//       second issuing thread: one thread issues about one MMA per 33 ns)
+//       second issuing thread: one thread issues about one MMA per 33 ns
+//       for any N up to 128)
 //   two row warpgroups (warps 4-7 and 8-11, thread = token row i = TMEM
 //       lane; warpgroup hf takes columns 64hf.. of P and dims 32hf.. of O):
 //       ReLU of Q and K in place (half of each row each); P -> A (causal
@@ -309,9 +310,10 @@ k_linattn(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtens
         }
     } else if (warp == 1 || warp == 2) {
         // ---------------- MMA issue: warp 1 MMA1, MMA3, MMA2; warp 2 MMA4 ----------------
-        // Two issuing threads: one thread issues an MMA about every 33 ns
-        // whatever its size, and MMA4 (the state update) and MMA2 (intra) are
-        // both narrow (N = 80), so together they keep the tensor pipe busier.
+        // Two issuing threads: one thread issues an MMA about every 33 ns for
+        // any N up to 128 (M = 128, K = 16), and MMA4 (the state update) and
+        // MMA2 (intra) are both narrow (N = 80), so together they keep the
+        // tensor pipe busier.
         // Descriptors of each operand's first K step are built once.  A step
         // of `off` bytes adds off >> 4 to the descriptor's start-address
         // field, which never carries out of it: every shared address here is

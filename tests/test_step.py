@@ -95,6 +95,49 @@ def test_steps_in_a_cuda_graph_match_plain_launches():
     assert torch.equal(O1, O2) and torch.equal(m1, m2) and torch.equal(u1, u2)
 
 
+@pytest.mark.parametrize("graph", [False, True])
+def test_step_reads_inputs_written_just_before_it(graph):
+    """Each step reads k_t and v_t from one buffer that a copy kernel refills
+    just before it on the same stream.  A step is launched as a programmatic
+    dependent of the kernel before it, so it must read only once that copy
+    has completed: the outputs equal those of steps reading every token's
+    inputs from their own rows."""
+    wl = inputs.custom(8, 8, 200, 64, seed=46, kind="stream")
+    q, K, V, n = stream_inputs(wl)
+    O_ref, m_ref, u_ref, w_ref = run_steps(q, K, V, n, torch.float32)
+    B, H, N, d = K.shape
+    qs = q.reshape(n, d).cuda()
+    Ks = K.permute(2, 0, 1, 3).reshape(N, n, d).contiguous().cuda()
+    Vs = V.permute(2, 0, 1, 3).reshape(N, n, d).contiguous().cuda()
+    kbuf = torch.empty(n, d, device="cuda")
+    vbuf = torch.empty(n, d, device="cuda")
+    Os = torch.empty((N, n, d), device="cuda")
+    m = torch.empty(n, device="cuda")
+    u = torch.empty(n, d, device="cuda")
+    w = torch.empty(n, device="cuda")
+
+    def body():
+        binding.aaren_state_init(m, u, w)
+        for t in range(N):
+            kbuf.copy_(Ks[t])
+            vbuf.copy_(Vs[t])
+            binding.aaren_step(qs, m, u, w, kbuf, vbuf, Os[t])
+
+    if graph:
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            body()
+        g.replay()
+    else:
+        body()
+    torch.cuda.synchronize()
+    assert binding.aaren_check() == 0
+    assert torch.equal(Os, O_ref)
+    assert torch.equal(m, m_ref) and torch.equal(u, u_ref) and torch.equal(w, w_ref)
+
+
 @pytest.mark.parametrize("d", [16, 32, 64, 128])
 @pytest.mark.parametrize("dt", ["f32", "bf16", "bf16_f32out"])
 def test_step_all_shapes(d, dt):
