@@ -240,15 +240,23 @@ __device__ __forceinline__ void chunk_aggregate(const float *wst, float &am,
 }
 
 // Decoupled look-back of chunk c (carry warp) whose fold reads the
-// predecessors' states through shared memory.  A window of 32 predecessors
-// is polled as in lookback(); once it resolves, the lanes of its first n
-// (up to FOLD) predecessors each start one 1-D bulk copy of their
-// state into the group's fold buffer `fb`, all on the mbarrier `fbar`, so
-// the whole window's states cross from L2 in one round trip and occupy no
-// registers while in flight (folding them from registers took one round
-// trip per batch of six states).  The fold itself then reads shared
-// memory.  The states are published with release semantics and their flags
-// read with acquire; a proxy fence orders those acquires before the copies.
+// predecessors' states through shared memory.  This kernel keeps the
+// chunks' aggregates in one array (states + chunk * SS) and their inclusive
+// prefixes in another (states + (chunks + chunk) * SS), so the aggregates of
+// consecutive predecessors are contiguous.  A window of 32 predecessors is
+// polled as in lookback(); once it resolves, every predecessor but the last
+// has only an aggregate, and the last may hold an inclusive prefix.  Lane 0
+// then starts at most two 1-D bulk copies per round of up to FOLD states
+// (the round's aggregates, in one piece, and the inclusive prefix) into the
+// group's fold buffer `fb`, on the mbarrier `fbar`: the states cross from L2
+// in one round trip and occupy no registers while in flight.  (A copy per
+// state cost more to issue than the round trip; splitting the aggregates
+// over several lanes' copies cost more in fences than it gained in landing
+// time; folding from registers took a round trip per six states.)  The fold then reads shared memory, in any
+// order of the states (one maximum over all of them, then a weighted sum).
+// The states are published with release semantics and the flags read with
+// acquire by each lane; the warp barrier orders those acquires before lane
+// 0's proxy fence and copies.
 // `fb_phase` is the parity of the fold barrier's next phase; `fb_busy` stays
 // true if a wait for copies gave up (the caller waits for them before the
 // block's shared memory can go).  False when a wait gave up or a
@@ -298,21 +306,29 @@ __device__ bool lookback_bulk(const ScanParams &p, int64_t head, int64_t c, floa
             __nanosleep(sleep_ns);
             if (sleep_ns < 256) sleep_ns *= 2;
         }
-        __syncwarp();   // every lane's acquire before any lane's copy
+        __syncwarp();   // every lane's acquire before lane 0's copies
         // predecessors 0..k of the window (lanes before chunk 0 are never
-        // copied: the first of them is the stop k, an identity)
+        // copied: the first of them is the stop k, an identity).  Predecessor
+        // i of the window is chunk j0 - i of the head.
         const int last = (j0 - k >= 0) ? k : static_cast<int>(j0);   // the window's last real predecessor
+        const size_t chunks = size_t(p.heads) * size_t(p.chunks_per_head);
         for (int i0 = 0; i0 <= last; i0 += FOLD) {
             const int n = (last + 1 - i0 < FOLD) ? last + 1 - i0 : FOLD;
-            const int i = i0 + lane;
-            const unsigned fi = __shfl_sync(kFull, f, i & 31);   // as lane i saw it
-            if (lane == 0) ptx::mbar_arrive_expect_tx(fbar, static_cast<unsigned>(n) * SS * sizeof(float));
-            __syncwarp();
-            if (lane < n) {
-                const float *src = p.states + (size_t(first + (j0 - i)) * 2 + (fi == FLAG_INC ? 1 : 0)) * SS;
+            // the round covers chunks j0 - i0 - n + 1 .. j0 - i0; only its
+            // last predecessor (the lowest chunk) can hold an inclusive prefix
+            const unsigned f_end = __shfl_sync(kFull, f, (i0 + n - 1) & 31);
+            const int n_inc = (f_end == FLAG_INC) ? 1 : 0;
+            const int n_agg = n - n_inc;
+            if (lane == 0) {
+                const size_t low = size_t(first + (j0 - i0 - n + 1));   // the round's lowest chunk
+                ptx::mbar_arrive_expect_tx(fbar, static_cast<unsigned>(n) * SS * sizeof(float));
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // earlier reads of fb first
                 ptx::fence_proxy_async_global();
-                ptx::bulk_g2s_plain(fb + lane * SS, src, SS * sizeof(float), fbar);
+                if (n_agg > 0)
+                    ptx::bulk_g2s_plain(fb, p.states + (low + n_inc) * SS,
+                                        static_cast<unsigned>(n_agg) * SS * sizeof(float), fbar);
+                if (n_inc)
+                    ptx::bulk_g2s_plain(fb + n_agg * SS, p.states + (chunks + low) * SS, SS * sizeof(float), fbar);
             }
             fb_busy = true;
             if (!wait_bar(fbar, fb_phase, wait_limit)) return false;
@@ -518,7 +534,8 @@ __global__ void __launch_bounds__(PipeTile<D, GROUPS, STAGES, Tin>::THREADS, 1)
             const bool publish = (chunk != p.fault_chunk) && slot_ok;
             bool issued = false;   // the group's next chunk was already started
             unsigned *my_flag = p.flags + chunk;
-            float *my_state = p.states + size_t(chunk) * 2 * SS;
+            // this chunk's inclusive prefix (its aggregate is at states + chunk * SS)
+            float *my_inc = p.states + (size_t(p.heads) * size_t(p.chunks_per_head) + size_t(chunk)) * SS;
 
             float xm = -INFINITY, xw = 0.f, xu[E];
 #pragma unroll
@@ -557,7 +574,7 @@ __global__ void __launch_bounds__(PipeTile<D, GROUPS, STAGES, Tin>::THREADS, 1)
                 issued = true;
                 combine_into<E>(xm, xu, xw, im, iu, iw);   // inclusive = exclusive (+) aggregate
                 if (publish) {
-                    write_state<D>(my_state + SS, im, iu, iw, lane);
+                    write_state<D>(my_inc, im, iu, iw, lane);
                     publish_flag(my_flag, FLAG_INC, lane);
                 }
                 if (c == p.chunks_per_head - 1 && p.m_out != nullptr) {
@@ -716,7 +733,7 @@ __global__ void __launch_bounds__(PipeTile<D, GROUPS, STAGES, Tin>::THREADS, 1)
                 if (lane == 0) ptx::mbar_arrive(cagg);
                 const int64_t chunk = head * p.chunks_per_head + c;
                 if (c > 0 && chunk != p.fault_chunk && rows_ok) {
-                    write_state<D>(p.states + size_t(chunk) * 2 * SS, am, au, aw, lane);
+                    write_state<D>(p.states + size_t(chunk) * SS, am, au, aw, lane);
                     publish_agg_if_none(p.flags + chunk, lane);
                 }
             }
