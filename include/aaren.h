@@ -85,6 +85,10 @@ typedef enum {
  * N = 0 (or B*H = 0) is a no-op.  The cross-block carry needs a workspace of
  * aaren_scan_workspace_bytes(B,H,N,d) bytes, taken from the stream-ordered
  * allocator (cudaMallocAsync / cudaFreeAsync on `stream`) for this call.
+ * Results are not bitwise reproducible from call to call: a chunk's carry
+ * combines whichever predecessors it finds holding only their own aggregate,
+ * so the grouping of the combining steps, and the last bits of O, depend on
+ * timing.  Every grouping is within the same error bound.
  * Errors: AAREN_ERR_INVALID, AAREN_ERR_UNSUPPORTED, AAREN_ERR_CUDA.
  */
 aaren_status_t aaren_scan_forward(const void *q, const void *K, const void *V,
@@ -160,7 +164,9 @@ aaren_status_t aaren_scan_forward_stats(const void *q, const void *K,
  * N = 0 writes dq = 0.  Errors: AAREN_ERR_INVALID, AAREN_ERR_UNSUPPORTED,
  * AAREN_ERR_CUDA, AAREN_ERR_WORKSPACE; device-side waits that give up are
  * reported by aaren_check().  dL/dq is summed with float32 atomics, so its
- * last bits may differ between runs.
+ * last bits may differ between runs; so may those of dK and dV, whose
+ * cross-block carry combines whichever successors it finds holding only
+ * their own aggregate (every grouping is within the same error bound).
  */
 aaren_status_t aaren_scan_backward(const void *q, const void *K, const void *V,
                                    const void *O, const void *dO,
