@@ -112,6 +112,38 @@ cudaError_t allow_smem(Kernel kern, size_t bytes, std::atomic<unsigned long long
     return e;
 }
 
+// A scan kernel launched as the programmatic dependent of the workspace
+// zeroing before it (k_zero_ws): its launch may begin while the zeroing runs;
+// the kernel waits for the zeroing's completion before any global access.
+template <typename... Args>
+cudaError_t launch_dependent(void (*kern)(Args...), unsigned grid, unsigned block, size_t smem,
+                             cudaStream_t st, Args... args)
+{
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
+// The ticket and flags of a scan workspace (bytes: a multiple of 16) zeroed
+// by k_zero_ws, in plain stream order.
+cudaError_t zero_scan_workspace(void *ws, size_t bytes, cudaStream_t st)
+{
+    const int64_t n16 = int64_t(bytes / 16);
+    int64_t blocks = (n16 + 255) / 256;
+    if (blocks > 1184) blocks = 1184;
+    if (blocks < 1) blocks = 1;
+    k_zero_ws<<<unsigned(blocks), 256, 0, st>>>(static_cast<uint4 *>(ws), n16);
+    return cudaGetLastError();
+}
+
 template <int D, typename Tin, typename Tout>
 aaren_status_t launch_scan(const ScanParams &p, int64_t total_chunks, cudaStream_t st)
 {
@@ -120,8 +152,9 @@ aaren_status_t launch_scan(const ScanParams &p, int64_t total_chunks, cudaStream
     static std::atomic<unsigned long long> configured{0};
     auto kern = k_scan_fwd<D, Tin, Tout, TC::WARPS, TC::GROUPS>;
     if (allow_smem(kern, Tile::smem_bytes, configured) != cudaSuccess) return AAREN_ERR_CUDA;
-    kern<<<unsigned(total_chunks), TC::WARPS * 32, Tile::smem_bytes, st>>>(p);
-    return cudaGetLastError() == cudaSuccess ? AAREN_OK : AAREN_ERR_CUDA;
+    return launch_dependent(kern, unsigned(total_chunks), TC::WARPS * 32, Tile::smem_bytes, st, p) == cudaSuccess
+               ? AAREN_OK
+               : AAREN_ERR_CUDA;
 }
 
 // Shape of the persistent bfloat16 kernel per d: groups (five warps each,
@@ -179,8 +212,10 @@ aaren_status_t launch_pipe(const ScanParams &p, int64_t total_chunks, cudaStream
     if (sms <= 0) return AAREN_ERR_CUDA;
     int64_t grid = int64_t(sms) * per_sm;
     if (grid > total_chunks) grid = total_chunks;
-    kern<<<unsigned(grid), Tile::THREADS, Tile::smem_bytes, st>>>(p, total_chunks);
-    return cudaGetLastError() == cudaSuccess ? AAREN_OK : AAREN_ERR_CUDA;
+    return launch_dependent(kern, unsigned(grid), Tile::THREADS, Tile::smem_bytes, st, p, total_chunks) ==
+                   cudaSuccess
+               ? AAREN_OK
+               : AAREN_ERR_CUDA;
 }
 
 template <int D>
@@ -604,7 +639,7 @@ static aaren_status_t scan_forward_impl(const void *q, const void *K, const void
         return AAREN_ERR_WORKSPACE;
     }
     aaren_status_t rc = AAREN_OK;
-    if (cudaMemsetAsync(ws, 0, wl.zero_bytes, st) != cudaSuccess) {
+    if (zero_scan_workspace(ws, wl.zero_bytes, st) != cudaSuccess) {
         rc = AAREN_ERR_CUDA;
     } else {
         unsigned *status = nullptr;
@@ -991,8 +1026,8 @@ extern "C" aaren_status_t aaren_scan_forward_noalloc(const void *q, const void *
     const aaren_status_t rc = noalloc_scratch(&scratch);
     if (rc != AAREN_OK) return rc;
     // The regular path with a caller workspace allocates nothing: it checks
-    // the pointers, zeroes the ticket and flags of the workspace
-    // (cudaMemsetAsync) and launches.
+    // the pointers, zeroes the ticket and flags of the workspace (a small
+    // kernel) and launches.
     return aaren_scan_forward_ex(q, K, V, O, B, H, N, d, dtype, nullptr, nullptr, nullptr, nullptr,
                                  nullptr, nullptr, scratch, AAREN_NOALLOC_SCRATCH_BYTES, stream);
 }

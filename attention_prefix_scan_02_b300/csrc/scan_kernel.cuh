@@ -73,6 +73,21 @@ struct ScanParams {
     int64_t wait_limit_ns;
 };
 
+// Zeroes the first n16 16-byte words of a scan workspace (the ticket and
+// the chunk flags).  The scan after it is launched as its programmatic
+// dependent: every block of this kernel lets that launch begin at once, so
+// the scan's blocks are placed and set up while the zeroing runs, and the
+// scan waits for this kernel's completion (griddepcontrol.wait) before its
+// first access to global memory.  This kernel itself is launched in plain
+// stream order, after everything before it (an earlier scan on the same
+// workspace included) has completed.
+__global__ void __launch_bounds__(256) k_zero_ws(uint4 *ws, int64_t n16)
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n16; i += int64_t(gridDim.x) * blockDim.x)
+        ws[i] = make_uint4(0u, 0u, 0u, 0u);
+}
+
 // Layout of one state in the workspace and in shared memory:
 // [m, w, unused, unused, u_0 .. u_{d-1}] (u 16-byte aligned).
 template <int D>
@@ -464,6 +479,9 @@ __global__ void __launch_bounds__(WARPS * 32)
     const int warp = tid >> 5;
     const int lane = tid & 31;
 
+    // launched as a programmatic dependent of the workspace zeroing: nothing
+    // in global memory is touched before that kernel has completed
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     if (tid == 0) {
         *s_chunk = static_cast<long long>(atomicAdd(p.ticket, 1u));
         *s_abort = 0;

@@ -429,6 +429,10 @@ __global__ void __launch_bounds__(PipeTile<D, GROUPS, STAGES, Tin>::THREADS, 1)
         ptx::mbar_init(fbar, 1);
     }
     if (threadIdx.x == 0) ptx::fence_barrier_init();
+    // launched as a programmatic dependent of the workspace zeroing: the set-up
+    // above overlaps it, and nothing in global memory is touched before it
+    // has completed
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     __syncthreads();
     // waits on the group's own barriers may legitimately last as long as a
     // look-back wait, so they get a wider limit

@@ -614,7 +614,9 @@ def run_ours(args):
         "dtype": "f32", "io_dtype": f"{wl.dtype} in, {out} out", "data": "synthetic",
         "config": dict(describe(wl, out), op=args.op, global_batch=world * wl.B,
                        parallelism=f"independent sequences, {world} rank(s), no collective"),
-        "gpu_launches": args.steps,
+        # a scan call launches the workspace zeroing (k_zero_ws) and the scan;
+        # the reduce and the backward zero theirs with a driver memset
+        "gpu_launches": args.steps if (reduce or backward) else 2 * args.steps,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "algorithmic_bytes_per_launch": alg_bytes, "launch_ms": mean_launch_ms,

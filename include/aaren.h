@@ -89,6 +89,10 @@ typedef enum {
  * combines whichever predecessors it finds holding only their own aggregate,
  * so the grouping of the combining steps, and the last bits of O, depend on
  * timing.  Every grouping is within the same error bound.
+ * A call launches two kernels on `stream`: one that zeroes the workspace's
+ * ticket and chunk flags, then the scan, launched as its programmatic
+ * dependent (its set-up overlaps the zeroing; it reads nothing before the
+ * zeroing has completed).
  * Errors: AAREN_ERR_INVALID, AAREN_ERR_UNSUPPORTED, AAREN_ERR_CUDA.
  */
 aaren_status_t aaren_scan_forward(const void *q, const void *K, const void *V,

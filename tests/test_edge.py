@@ -178,3 +178,44 @@ def test_streams_are_respected():
         O = binding.scan_forward(qg, Kg, Vg, out_dtype=torch.float32)
     assert binding.aaren_check(s) == 0
     assert rowwise_rel(O.cpu(), oracle_all(q, K, V)[0]) <= TOL_BF16
+
+
+@pytest.mark.parametrize("graph", [False, True])
+def test_scan_reads_inputs_written_just_before_it(graph):
+    """Two scans on one workspace, each reading q, K and V from buffers that
+    copy kernels refill just before it on the same stream.  The scan kernel
+    is launched as a programmatic dependent of its workspace zeroing, which
+    itself follows the copies in stream order, so the scan must read nothing
+    before the copies (and the earlier scan's use of the workspace) are
+    complete: each output matches the oracle on its own inputs."""
+    d, N = 64, 5 * 128 + 17
+    sets = [make(2, 3, N, d, "bf16", seed=s) for s in (61, 62)]
+    refs = [oracle_all(q, K, V) for q, K, V in sets]
+    dev = [tuple(t.cuda() for t in s) for s in sets]
+    qb = torch.empty_like(dev[0][0])
+    Kb = torch.empty_like(dev[0][1])
+    Vb = torch.empty_like(dev[0][2])
+    outs = [torch.empty(Kb.shape, dtype=torch.float32, device="cuda") for _ in sets]
+    states = [tuple(torch.empty(s, device="cuda") for s in ((2, 3), (2, 3, d), (2, 3))) for _ in sets]
+    ws = torch.empty(binding.aaren_scan_workspace_bytes(2, 3, N, d), dtype=torch.uint8, device="cuda")
+
+    def body():
+        for (q, K, V), O, (m, u, w) in zip(dev, outs, states):
+            qb.copy_(q)
+            Kb.copy_(K)
+            Vb.copy_(V)
+            binding.aaren_scan_forward_ex(qb, Kb, Vb, O, m_out=m, u_out=u, w_out=w, workspace=ws)
+
+    if graph:
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            body()
+        g.replay()
+    else:
+        body()
+    torch.cuda.synchronize()
+    assert binding.aaren_check() == 0
+    for O, st, ref in zip(outs, states, refs):
+        compare(O, st, ref, TOL_BF16, False)
